@@ -1,0 +1,50 @@
+"""CPU oracle for the Muon optimizer step -- TEST INFRASTRUCTURE ONLY.
+
+This package is a plain, slow, obviously correct NumPy restatement of the Muon
+step (Nesterov momentum, quintic Newton-Schulz orthogonalisation, parameter
+update).  It exists to check the CUDA path and to serve as the timed CPU
+baseline.  Only the test-suite, the smoke check and the benchmark's CPU-baseline
+and reference legs may import it; the product path never does, and it shares no
+code with the CUDA kernels.
+
+Source of the method:
+  page "深入解析KellerJordan/modded-nanogpt中的训练架构与优化技术"
+  (reposource.net, an annotated walk-through of modded-nanogpt's train_gpt.py),
+  sections "Muon优化器：动量正交化技术" (the Muon class and its defaults) and
+  "Newton-Schulz正交化" (the function zeropower_via_newtonschulz5 and its
+  coefficients).
+
+Three steps are not printed on that page; the readings taken here are stated in
+``oracle.muon`` next to the code that takes them.
+
+Pin status: every public function is pinned by the CPU tests
+(closed form via SVD, invariants, brute force in exact rational arithmetic,
+bit-exact bf16 rounding against an independent routine).
+"""
+
+from .bf16 import round_to_bf16, BF16_MAX
+from .muon import (
+    NS_COEFFS,
+    NORM_EPS,
+    MUON_DEFAULTS,
+    momentum_update,
+    orient,
+    normalise,
+    ns_iteration,
+    newton_schulz5,
+    muon_step,
+)
+
+__all__ = [
+    "round_to_bf16",
+    "BF16_MAX",
+    "NS_COEFFS",
+    "NORM_EPS",
+    "MUON_DEFAULTS",
+    "momentum_update",
+    "orient",
+    "normalise",
+    "ns_iteration",
+    "newton_schulz5",
+    "muon_step",
+]
