@@ -1,0 +1,433 @@
+"""Benchmark of the Muon step on GB300 (one JSON line on rank 0).
+
+Workload (default ``gpt2``): the GPT-2-124M hidden-matrix bank -- 12 layers of
+q, k, v, o (768x768), c_fc (3072x768), c_proj (768x3072): 72 matrices, 84.93 M
+fp32 parameters, bf16 gradients, fp32 momentum buffers -- with fresh seeded
+gradients every step (three gradient sets, used in turn).  One step = one full
+Muon step over the bank: momentum, normalisation, 5 quintic Newton-Schulz
+steps, parameter update (17 kernel launches through the C ABI).
+
+  value      matrices per second, device-timed with CUDA events on the
+             launching stream, inputs resident in HBM (the bank's 0.85 GB of
+             inputs exceed the 129 MB L2, so no flush between steps)
+  e2e        the same metric through the public API with host buffers: each
+             step copies that step's gradients host->device from pinned memory
+             and reads the updated parameters back device->host
+  roofline   the dominant kernel (largest share of device time), its
+             algorithmic FLOPs (or bytes) per launch over its live average
+             launch time, against MEASURED_PEAKS.json
+  cpu_baseline  the CPU oracle (bf16-emulating mode) timed on the host cores
+             on a bounded sample of the bank's matrices
+
+``--impl reference`` times the CPU oracle as the reference arm (rank 0 only).
+Multi-GPU (torchrun): every rank updates its own replica of the bank (the
+step does not shard); value = matrices of all ranks / max time over ranks.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+LR, MU, NS_STEPS = 0.02, 0.95, 5
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------------ workloads
+def workload_shapes(name):
+    from newton_schulz_08_gb300 import inputs
+    return {
+        "gpt2": inputs.gpt2_shapes(),
+        "gpt1p5b": inputs.gpt1p5b_shapes(),
+        "rect": inputs.rect_shapes(),
+        "single": [inputs.SINGLE["shape"]],
+    }[name]
+
+
+WORKLOAD_DESC = {
+    "gpt2": "GPT-2-124M hidden-matrix bank: 12 x {4 x 768x768, 3072x768, 768x3072}, 72 matrices, "
+            "84.93M fp32 params, bf16 grads (fresh each step), fp32 momentum",
+    "gpt1p5b": "1.5B-shaped bank: 48 x {4 x 1600x1600, 6400x1600, 1600x6400}, 288 matrices, "
+               "1.4746B fp32 params, bf16 grads, fp32 momentum",
+    "rect": "rectangular bank: 8 each of 1024x4096, 4096x1024, 768x3072, 2048x8192, bf16 grads",
+    "single": "single 128x512 matrix, fp32 grad",
+}
+
+
+def ns_flops(shapes, steps=NS_STEPS):
+    """Algorithmic FLOPs per kernel kind for one step over the bank."""
+    f = {"gram": 0.0, "poly": 0.0, "update": 0.0}
+    for r, c in shapes:
+        m, n = min(r, c), max(r, c)
+        f["gram"] += float(m) * (m + 1) * n
+        f["poly"] += float(m) * m * (m + 1)
+        f["update"] += 2.0 * m * m * n
+    return {k: v * steps for k, v in f.items()}
+
+
+def hbm_bytes(shapes, gbytes):
+    """Algorithmic bytes of the elementwise passes for one step over the bank."""
+    e = float(sum(r * c for r, c in shapes))
+    return {"momentum_cast": e * (gbytes + 4 + 4 + 2),  # g, buf r/w, Xraw
+            "normalise": e * 4}                          # Xraw r, X0 w
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def oracle_sample(shapes, budget_s, min_mats=1, mode="bf16"):
+    """Time the oracle's Muon step on matrices of the bank taken in order
+    (wrapping around) until `budget_s` seconds have passed."""
+    import oracle
+    from newton_schulz_08_gb300 import inputs
+    done, t_total, i = 0, 0.0, 0
+    while done < min_mats or t_total < budget_s:
+        shape = shapes[i % len(shapes)]
+        p = inputs.param(shape, i)
+        g = oracle.round_to_bf16(inputs.grad(shape, i)).astype(np.float32)
+        b = inputs.buffer(shape, i)
+        t0 = time.perf_counter()
+        oracle.muon_step(p, g, b, LR, MU, True, NS_STEPS, mode)
+        t_total += time.perf_counter() - t0
+        done += 1
+        i += 1
+    return done, t_total
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the CPU oracle, as it stands, on the host cores."""
+    if rank != 0:
+        return
+    shapes = workload_shapes(args.workload)
+    # size each step so the whole run stays within about two minutes
+    n0, t0 = oracle_sample(shapes, 0.0, min_mats=1)
+    per_mat = t0 / n0
+    per_step_budget = max(per_mat, 120.0 / max(1, args.steps + args.warmup))
+    mats_per_step = max(1, int(per_step_budget / per_mat))
+    for _ in range(args.warmup):
+        oracle_sample(shapes, 0.0, min_mats=mats_per_step)
+    total_mats, total_t = 0, 0.0
+    for _ in range(args.steps):
+        n, t = oracle_sample(shapes, 0.0, min_mats=mats_per_step)
+        total_mats += n
+        total_t += t
+    value = total_mats / total_t
+    sample = f"{mats_per_step} matrices of the bank per step (bf16-emulating oracle, taken in bank order)"
+    line = {
+        "impl": "reference", "metric": "muon_step_matrices_per_s", "value": value,
+        "unit": "matrices/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * total_t / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (bf16-emulating)",
+        "data": "synthetic", "config": {"workload": WORKLOAD_DESC[args.workload]},
+        "cpu_baseline": {"value": value, "unit": "matrices/s", "cores": cpu_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "matrices/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+def build_bank(shapes, device, grad_sets):
+    """Device tensors of the bank: params, bufs, grad sets (flat + views)."""
+    import torch
+    from newton_schulz_08_gb300 import inputs
+    sizes = [r * c for r, c in shapes]
+    total = sum(sizes)
+    P = torch.empty(total, dtype=torch.float32, device=device)
+    Bf = torch.empty(total, dtype=torch.float32, device=device)
+    Gs_host = [torch.empty(total, dtype=torch.bfloat16).pin_memory() for _ in range(grad_sets)]
+    off = 0
+    for i, (shape, sz) in enumerate(zip(shapes, sizes)):
+        P[off:off + sz].copy_(torch.from_numpy(inputs.param(shape, i).ravel()))
+        Bf[off:off + sz].copy_(torch.from_numpy(inputs.buffer(shape, i).ravel()))
+        for k in range(grad_sets):
+            Gs_host[k][off:off + sz].copy_(torch.from_numpy(inputs.grad(shape, i, step=k).ravel()))
+        off += sz
+    Gs = [g.to(device) for g in Gs_host]
+    return P, Bf, Gs, Gs_host
+
+
+def views(flat, shapes):
+    out, off = [], 0
+    for r, c in shapes:
+        out.append(flat[off:off + r * c].view(r, c))
+        off += r * c
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="gpt2", choices=sorted(WORKLOAD_DESC))
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of CPU oracle work")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import ctypes
+
+    import torch
+    import torch.distributed as dist
+
+    from newton_schulz_08_gb300 import muon
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+
+    L = muon.lib()
+    shapes = workload_shapes(args.workload)
+    grad_sets = 3
+    P, Bf, Gs, Gs_host = build_bank(shapes, device, grad_sets)
+    Pv, Bv = views(P, shapes), views(Bf, shapes)
+    descs = []
+    for k in range(grad_sets):
+        arr, n = muon._descs(Pv, views(Gs[k], shapes), Bv)
+        descs.append(arr)
+    n_mats = len(shapes)
+    ws = muon.new_workspace(L.muon_workspace_size(descs[0], n_mats), device)
+    ws_ptr, ws_bytes = ctypes.c_void_p(ws.data_ptr()), ws.numel()
+    stream = torch.cuda.current_stream(device)
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+
+    def step(k):
+        st = L.muon_step(descs[k % grad_sets], n_mats, LR, MU, 1, NS_STEPS, ws_ptr, ws_bytes, sptr)
+        if st != 0:
+            raise muon.MuonError(st, "muon_step")
+
+    def barrier():
+        torch.cuda.synchronize(device)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(device)
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    for k in range(args.warmup):
+        step(k)
+    barrier()
+    st = muon.muon_device_status(ws)
+    if st != 0:
+        raise muon.MuonError(st, "device status after warm-up")
+
+    # -------------------------------------------------------------- timed
+    clocks = ClockSampler(local)
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for k in range(args.steps):
+        step(k)
+    e1.record(stream)
+    barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+
+    # ---------------------------------------------- per-kernel live timing
+    muon.muon_set_debug("record_kernel_events", 1)
+    muon.muon_kernel_times()
+    for k in range(args.steps):
+        step(k)
+    barrier()
+    ktimes = muon.muon_kernel_times()
+    muon.muon_set_debug("record_kernel_events", 0)
+
+    # ------------------------------------------------------------- e2e
+    Gh_dev = Gs[0]
+    P_host = torch.empty(P.numel(), dtype=torch.float32).pin_memory()
+    e_steps = max(3, args.steps // 4)
+    barrier()
+    e0.record(stream)
+    for k in range(e_steps):
+        Gh_dev.copy_(Gs_host[k % grad_sets], non_blocking=True)
+        st_ = L.muon_step(descs[0], n_mats, LR, MU, 1, NS_STEPS, ws_ptr, ws_bytes, sptr)
+        if st_ != 0:
+            raise muon.MuonError(st_, "muon_step")
+        P_host.copy_(P, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps)
+    st = muon.muon_device_status(ws)
+    if st != 0:
+        raise muon.MuonError(st, "device status after timing")
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    # ------------------------------------------------------------- report
+    peaks, peak_src = load_peaks()
+    flops = ns_flops(shapes)
+    gbytes = hbm_bytes(shapes, 2)
+    kern = {}
+    for kind, (tot_ms, cnt) in ktimes.items():
+        if cnt == 0:
+            continue
+        avg = tot_ms / cnt
+        per_step = cnt / args.steps
+        if kind in flops:
+            work = flops[kind] / per_step  # per launch
+            ach = work / (avg * 1e-3) / 1e12
+            kern[kind] = {"avg_ms": avg, "launches_per_step": per_step, "share": None,
+                          "achieved": ach, "unit": "TFLOP/s", "bound": "tensor",
+                          "peak": peaks["bf16_tflops"], "frac": ach / peaks["bf16_tflops"],
+                          "work_per_launch": work}
+        else:
+            work = gbytes[kind] / per_step
+            ach = work / (avg * 1e-3) / 1e9
+            kern[kind] = {"avg_ms": avg, "launches_per_step": per_step, "share": None,
+                          "achieved": ach, "unit": "GB/s", "bound": "hbm",
+                          "peak": peaks["hbm_gbs"], "frac": ach / peaks["hbm_gbs"],
+                          "work_per_launch": work}
+    tot = sum(v["avg_ms"] * v["launches_per_step"] for v in kern.values())
+    for v in kern.values():
+        v["share"] = v["avg_ms"] * v["launches_per_step"] / tot
+    dom = max(kern, key=lambda k: kern[k]["share"])
+    d = kern[dom]
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tfile):
+        with open(tfile) as f:
+            traffic = json.load(f).get(args.workload, {}).get(dom)
+
+    value = n_mats * world / (ms * 1e-3)
+    total_flops = sum(flops.values())
+    line = {
+        "metric": "muon_step_matrices_per_s", "value": value, "unit": "matrices/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC[args.workload], "matrices": n_mats,
+                   "params": int(sum(r * c for r, c in shapes)), "ns_steps": NS_STEPS,
+                   "lr": LR, "momentum": MU, "nesterov": True,
+                   "l2": "no flush: inputs (params, bufs, grads) exceed the 129 MB L2",
+                   "parallelism": f"replicas x{world}"},
+        "ns5_tflops": total_flops / (ms * 1e-3) / 1e12,
+        "ns5_tflops_note": "algorithmic NS FLOPs of the whole step / step time",
+        "update_gbs": (gbytes["momentum_cast"] + 8.0 * sum(r * c for r, c in shapes)) / (ms * 1e-3) / 1e9,
+        "roofline": {"kernel": dom, "bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"],
+                     "unit": d["unit"], "frac": d["frac"], "traffic": traffic,
+                     "peak_source": f"{peak_src} ({'bf16_tflops burst' if d['unit'] == 'TFLOP/s' else 'hbm_gbs'})"},
+        "kernels": kern,
+        "e2e": {"value": n_mats * world / (e2e_ms * 1e-3), "unit": "matrices/s",
+                "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": int(Gs_host[0].numel() * 2),
+                "d2h_bytes_per_step": int(P_host.numel() * 4)},
+        "gpu_launches": int(sum(c for _, c in ktimes.values())),
+        "gpu_launches_note": "kernels launched in the per-kernel timing pass (same count as the main timed loop)",
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        n_cpu, t_cpu = oracle_sample(shapes, args.cpu_budget)
+        line["cpu_baseline"] = {"value": n_cpu / t_cpu, "unit": "matrices/s", "cores": cpu_threads(),
+                                "kind": "oracle",
+                                "sample": f"{n_cpu} matrices of the bank in order, full Muon step, "
+                                          f"bf16-emulating oracle, {t_cpu:.1f} s"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,161 @@
+/*
+ * muon.h -- C ABI of libmuon.so: the Muon optimizer step on one GB300 GPU
+ * (sm_103a).
+ *
+ * The method is the one the page "深入解析KellerJordan/modded-nanogpt中的训练架构
+ * 与优化技术" (reposource.net) walks through:
+ *   - section "Muon优化器：动量正交化技术": Muon = SGD momentum followed by
+ *     orthogonalisation of the update with a Newton-Schulz iteration;
+ *     constructor defaults lr = 0.02, momentum = 0.95, nesterov = True,
+ *     ns_steps = 5; step(): momentum update, Newton-Schulz, parameter update.
+ *   - section "Newton-Schulz正交化": zeropower_via_newtonschulz5(G, steps):
+ *     X = G in bfloat16, then `steps` times A = X X^T, B = b A + c A A,
+ *     X = a X + B X with (a, b, c) = (3.4445, -4.7750, 2.0315).
+ * Readings of what that page leaves out (fixed here):
+ *   - momentum: buf <- mu*buf + g; Nesterov: u <- g + mu*buf (new buf),
+ *     otherwise u <- buf;
+ *   - before iterating, X <- X / (||X||_F + 1e-7), the norm of the bfloat16 X,
+ *     the quotient rounded to bfloat16;
+ *   - a matrix with more rows than columns is transposed before iterating and
+ *     transposed back after, so the Gram matrix A is min(R,C) square;
+ *   - update: p <- p - lr * O (no weight decay, no shape-dependent lr).
+ * Each of A, B and X is rounded once to bfloat16 (round to nearest even)
+ * after its statement; products accumulate in fp32 on the tensor cores.
+ *
+ * Conventions for every entry point:
+ *   - Matrices are row-major and contiguous: element (i, j) of an R x C
+ *     matrix is at offset i*C + j.
+ *   - All data pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates, frees or keeps device memory between calls.  `stream`
+ *     is a cudaStream_t (NULL = legacy default stream) owned by the caller.
+ *   - Calls are asynchronous on `stream` and never synchronise, except
+ *     muon_device_status().  A workspace must not be shared by calls that
+ *     may overlap on the GPU.
+ *   - Arguments are checked on the host before anything is launched; on any
+ *     error code nothing has been enqueued and no buffer has been touched.
+ *   - Device-side conditions (a non-finite norm, an expired bounded wait)
+ *     are recorded in the workspace's status word and are read with
+ *     muon_device_status().
+ */
+#ifndef MUON_H
+#define MUON_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum muon_status {
+  MUON_OK = 0,
+  MUON_WARN_NONFINITE = 1,          /* a matrix had a non-finite norm; values propagate */
+  MUON_ERR_INVALID_ARG = -1,        /* null pointer, size <= 0, bad dtype, ns_steps < 0 */
+  MUON_ERR_MISALIGNED = -2,         /* a data pointer is not 16-byte aligned */
+  MUON_ERR_ALIASING = -3,           /* byte ranges that are written overlap another operand */
+  MUON_ERR_WORKSPACE_TOO_SMALL = -4,
+  MUON_ERR_CUDA = -5,               /* a CUDA runtime call or launch failed */
+  MUON_ERR_DEVICE_TIMEOUT = -6,     /* a bounded on-device wait expired (results invalid) */
+  MUON_ERR_UNSUPPORTED_DEVICE = -7, /* the current device is not compute capability 10.3 */
+  MUON_ERR_TOO_LARGE = -8           /* a dimension exceeds 2^31-1 elements per row/matrix */
+} muon_status_t;
+
+typedef enum muon_dtype { MUON_BF16 = 0, MUON_F32 = 1 } muon_dtype_t;
+
+/* One 2-D weight matrix of a bank (the unit the Muon class's step() updates). */
+typedef struct muon_mat_desc {
+  float* param;        /* R x C fp32, updated in place: p <- p - lr * O */
+  const void* grad;    /* R x C gradient, read only, dtype = grad_dtype */
+  float* buf;          /* R x C fp32 momentum buffer, updated in place */
+  int64_t rows, cols;  /* R, C > 0 */
+  int32_t grad_dtype;  /* muon_dtype_t */
+  int32_t reserved;    /* must be 0 */
+} muon_mat_desc;
+
+/* Bytes of device workspace muon_step needs for this bank (0 on invalid
+ * arguments).  Depends only on the shapes. */
+size_t muon_workspace_size(const muon_mat_desc* mats, int n_mats);
+
+/* One Muon step on a bank of matrices (page above, section "Muon优化器：
+ * 动量正交化技术", step(): momentum, Newton-Schulz, update).
+ *   mats      host array of n_mats descriptors (read during the call only);
+ *             param/grad/buf must be 16-byte aligned and must not overlap
+ *             each other or another matrix's param/buf.
+ *   lr, momentum, nesterov   as in the Muon constructor (nesterov 0 or 1).
+ *   ns_steps  Newton-Schulz steps (>= 0; 0 gives O = X0).
+ *   workspace device memory of at least muon_workspace_size() bytes,
+ *             256-byte aligned; its contents on entry do not matter.
+ * Matrices of equal (min(R,C), max(R,C)) form one shape class; each
+ * Newton-Schulz phase runs as one persistent launch over all classes. */
+muon_status_t muon_step(const muon_mat_desc* mats, int n_mats, float lr, float momentum,
+                        int nesterov, int ns_steps, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/* Bytes of device workspace ns5 needs. */
+size_t ns5_workspace_size(int batch, int64_t rows, int64_t cols);
+
+/* zeropower_via_newtonschulz5 (page above, section "Newton-Schulz正交化") on a
+ * strided batch: G is batch x rows x cols (dtype g_dtype), O is the same
+ * shape in bfloat16 (written).  No momentum.  G and O must be 16-byte aligned
+ * and must not overlap. */
+muon_status_t ns5(const void* G, int g_dtype, void* O, int batch, int64_t rows, int64_t cols,
+                  int ns_steps, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Same as ns5 for a list of differently shaped matrices G[i] -> O[i]
+ * (rows[i] x cols[i]); one launch per phase for the whole list. */
+muon_status_t ns5_bank(const void* const* G, const int32_t* g_dtype, void* const* O,
+                       const int64_t* rows, const int64_t* cols, int n_mats, int ns_steps,
+                       void* workspace, size_t workspace_bytes, void* stream);
+size_t ns5_bank_workspace_size(const int64_t* rows, const int64_t* cols, int n_mats);
+
+/* Synchronises `stream`, then reads the status word of `workspace` left by
+ * the last call that used it: MUON_OK, MUON_WARN_NONFINITE or
+ * MUON_ERR_DEVICE_TIMEOUT (MUON_ERR_CUDA if the synchronisation failed). */
+muon_status_t muon_device_status(const void* workspace, void* stream);
+
+/* Static description of a status code. */
+const char* muon_status_str(muon_status_t status);
+
+/* Where ns5 keeps its bfloat16 buffers inside the workspace (for tests and
+ * inspection): byte offsets of the two X buffers, of A and of B, the row
+ * pitches in elements, and m = min(rows, cols), n = max(rows, cols).  After
+ * ns5 with ns_steps = k >= 1: A and B hold step k's values, and X buffer
+ * (k % 2) holds step k's X (m x n, transposed for tall input); with k = 0,
+ * X buffer 0 holds X0. */
+typedef struct muon_ws_layout {
+  size_t x_offset[2];
+  size_t a_offset;
+  size_t b_offset;
+  int64_t ldx, lda;
+  int64_t m, n;
+} muon_ws_layout;
+muon_status_t ns5_workspace_layout(int batch, int64_t rows, int64_t cols, muon_ws_layout* out);
+
+/* Process-wide knobs for tests and diagnostics.  Keys:
+ *   "wait_budget_cycles"  clock64 cycles a kernel waits on one barrier
+ *                         before giving up (default 4e9, about 2 s);
+ *   "inject_stall"        1: the Newton-Schulz kernels' MMA warp issues
+ *                         nothing, so their waits expire (tests the bounded
+ *                         wait path; combine with a small budget);
+ *   "store_final_x"       1: the last B*X launch also stores the final X in
+ *                         the workspace (as ns5_workspace_layout describes);
+ *   "record_kernel_events" 1: every kernel launch is bracketed by a pair of
+ *                         CUDA events recorded on the caller's stream (read
+ *                         with muon_kernel_times; not for use under stream
+ *                         capture).
+ * Returns 0 on success, -1 for an unknown key. */
+int muon_set_debug(const char* key, long long value);
+
+/* Waits for the events recorded since the last call (see
+ * "record_kernel_events") and returns, per kernel kind, the summed
+ * milliseconds and the launch count: kind 0 momentum_cast, 1 normalise,
+ * 2 Gram (A = X X^T), 3 polynomial (B = b A + c A A), 4 update
+ * (X = a X + B X).  ms and launches are host arrays of n_kinds entries.
+ * Returns 0, or -1 on a bad argument or a failed event query. */
+int muon_kernel_times(double* ms, int* launches, int n_kinds);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MUON_H */

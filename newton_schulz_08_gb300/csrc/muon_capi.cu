@@ -1,0 +1,710 @@
+// C ABI of libmuon.so (declared in include/muon.h): argument checks, the bank
+// planner (shape classes, workspace layout, tile lists), TMA descriptor
+// encoding and the launch sequence of one Muon step / one Newton-Schulz call.
+//
+// Launch sequence (all on the caller's stream, nothing synchronises):
+//   memset(status word)
+//   momentum_cast      1 launch per 96 matrices: momentum, bf16 cast,
+//                      transpose of tall matrices, partial norms
+//   normalise          1 launch: X0 = bf16(Xraw / (||Xraw||_F + 1e-7))
+//   ns_steps x { Gram, Poly, Update }   1 persistent launch each for the
+//                      whole bank (per group of <= 8 shape classes); the last
+//                      Update applies p <- p - lr O (or writes O).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <climits>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/muon.h"
+#include "plan.h"
+
+namespace muon {
+
+cudaError_t launch_ns_gemm(int mode, const GemmParams& P, int num_sms, cudaStream_t stream);
+cudaError_t launch_momentum_cast(const K1Params& P, int blocks, cudaStream_t stream);
+cudaError_t launch_normalise(const NormParams& P, int blocks, cudaStream_t stream);
+
+namespace {
+
+// Newton-Schulz coefficients (a, b, c), section "Newton-Schulz正交化".
+constexpr float kCoefA = 3.4445f;
+constexpr float kCoefB = -4.7750f;
+constexpr float kCoefC = 2.0315f;
+
+constexpr size_t kAlign = 1024;
+constexpr int kElemsPerBlock = 16384;  // elementwise passes: ~16K elements per block
+
+std::atomic<long long> g_wait_budget{4000000000LL};
+std::atomic<int> g_inject_stall{0};
+std::atomic<int> g_store_final_x{0};
+std::atomic<int> g_record_events{0};
+
+// Optional CUDA-event brackets around every launch (diagnostics).
+constexpr int kKinds = 5;  // momentum_cast, normalise, gram, poly, update
+struct EventPair {
+  cudaEvent_t start, stop;
+  int kind;
+};
+std::mutex g_ev_mu;
+std::vector<EventPair> g_ev_pending;
+std::vector<EventPair> g_ev_pool;
+
+bool ev_begin(EventPair& e, int kind, cudaStream_t s) {
+  if (!g_record_events.load()) return false;
+  {
+    std::lock_guard<std::mutex> lk(g_ev_mu);
+    if (!g_ev_pool.empty()) {
+      e = g_ev_pool.back();
+      g_ev_pool.pop_back();
+    } else {
+      if (cudaEventCreate(&e.start) != cudaSuccess) return false;
+      if (cudaEventCreate(&e.stop) != cudaSuccess) return false;
+    }
+  }
+  e.kind = kind;
+  return cudaEventRecord(e.start, s) == cudaSuccess;
+}
+
+void ev_end(EventPair& e, bool active, cudaStream_t s) {
+  if (!active) return;
+  cudaEventRecord(e.stop, s);
+  std::lock_guard<std::mutex> lk(g_ev_mu);
+  g_ev_pending.push_back(e);
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+// One matrix of a job, whatever the entry point.
+struct JobMat {
+  const void* g;
+  int g_f32;
+  float* buf;   // null: no momentum
+  void* out;    // param (fp32) or O (bf16)
+  long long R, C;
+};
+
+struct ClassPlan {
+  int m, n, count;
+  int ldx, lda;
+  size_t x_off[2], a_off, b_off;
+  int mat_begin;  // position in class order
+  int norm_rpb, norm_blocks;
+};
+
+struct Plan {
+  std::vector<ClassPlan> cls;
+  std::vector<int> order;  // class order -> job index
+  std::vector<int> part_off, nparts, k1_rpb;
+  size_t parts_off = 0, table_off = 0, total = 0;
+  int total_parts = 0;
+};
+
+bool build_plan(const std::vector<JobMat>& mats, Plan& P) {
+  const int N = static_cast<int>(mats.size());
+  std::vector<int> cls_of(N);
+  for (int i = 0; i < N; ++i) {
+    const long long m = std::min(mats[i].R, mats[i].C), n = std::max(mats[i].R, mats[i].C);
+    int c = -1;
+    for (size_t k = 0; k < P.cls.size(); ++k)
+      if (P.cls[k].m == m && P.cls[k].n == n) c = static_cast<int>(k);
+    if (c < 0) {
+      ClassPlan cp{};
+      cp.m = static_cast<int>(m);
+      cp.n = static_cast<int>(n);
+      cp.count = 0;
+      P.cls.push_back(cp);
+      c = static_cast<int>(P.cls.size()) - 1;
+    }
+    cls_of[i] = c;
+    P.cls[c].count++;
+  }
+  for (size_t c = 0; c < P.cls.size(); ++c) {
+    P.cls[c].mat_begin = static_cast<int>(P.order.size());
+    for (int i = 0; i < N; ++i)
+      if (cls_of[i] == static_cast<int>(c)) P.order.push_back(i);
+  }
+  // partial sums of the momentum pass
+  P.part_off.resize(N);
+  P.nparts.resize(N);
+  P.k1_rpb.resize(N);
+  int parts = 0;
+  for (int k = 0; k < N; ++k) {
+    const JobMat& M = mats[P.order[k]];
+    int rpb, blocks;
+    if (M.R > M.C) {
+      rpb = 64;
+      blocks = static_cast<int>(ceil_div(M.R, 64));
+    } else {
+      rpb = static_cast<int>(std::max<long long>(1, kElemsPerBlock / M.C));
+      blocks = static_cast<int>(ceil_div(M.R, rpb));
+    }
+    P.k1_rpb[k] = rpb;
+    P.part_off[k] = parts;
+    P.nparts[k] = blocks;
+    if (parts > INT_MAX - blocks) return false;
+    parts += blocks;
+  }
+  P.total_parts = parts;
+  size_t off = 256;  // header: status word
+  P.parts_off = off;
+  off = align_up(off + sizeof(float) * static_cast<size_t>(parts), kAlign);
+  P.table_off = off;
+  off = align_up(off + sizeof(MatInfo) * static_cast<size_t>(N), kAlign);
+  for (ClassPlan& cp : P.cls) {
+    cp.ldx = static_cast<int>(align_up(cp.n, 8));
+    cp.lda = static_cast<int>(align_up(cp.m, 8));
+    const size_t xb = sizeof(__nv_bfloat16) * static_cast<size_t>(cp.count) * cp.m * cp.ldx;
+    const size_t ab = sizeof(__nv_bfloat16) * static_cast<size_t>(cp.count) * cp.m * cp.lda;
+    cp.x_off[0] = off;
+    off = align_up(off + xb, kAlign);
+    cp.x_off[1] = off;
+    off = align_up(off + xb, kAlign);
+    cp.a_off = off;
+    off = align_up(off + ab, kAlign);
+    cp.b_off = off;
+    off = align_up(off + ab, kAlign);
+    cp.norm_rpb = static_cast<int>(std::max(1, kElemsPerBlock / cp.n));
+    cp.norm_blocks = static_cast<int>(ceil_div(cp.m, cp.norm_rpb));
+  }
+  P.total = off;
+  return true;
+}
+
+// ------------------------------------------------------------------- checks
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Range {
+  uintptr_t lo, hi;
+  bool written;
+};
+
+bool ranges_overlap(std::vector<Range>& r) {
+  std::sort(r.begin(), r.end(), [](const Range& a, const Range& b) { return a.lo < b.lo; });
+  uintptr_t max_all = 0, max_written = 0;
+  for (const Range& x : r) {
+    if (x.lo < max_written) return true;
+    if (x.written && x.lo < max_all) return true;
+    max_all = std::max(max_all, x.hi);
+    if (x.written) max_written = std::max(max_written, x.hi);
+  }
+  return false;
+}
+
+muon_status_t check_shapes(long long R, long long C) {
+  if (R <= 0 || C <= 0) return MUON_ERR_INVALID_ARG;
+  if (R > INT_MAX || C > INT_MAX) return MUON_ERR_TOO_LARGE;
+  // per-matrix element counts and tile indices stay within int / TMA limits
+  if (R * C > (1LL << 40)) return MUON_ERR_TOO_LARGE;
+  const long long m = std::min(R, C);
+  if (ceil_div(m, kBM) * ceil_div(std::max(R, C), kBN) > (1LL << 24)) return MUON_ERR_TOO_LARGE;
+  return MUON_OK;
+}
+
+// ----------------------------------------------------------------- devices
+struct DeviceInfo {
+  int ok = -1;  // -1 unknown, 0 unsupported, 1 sm_103
+  int sms = 0;
+};
+
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+
+muon_status_t current_device(int& sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MUON_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (dev < 0 || dev >= 64) return MUON_ERR_UNSUPPORTED_DEVICE;
+  DeviceInfo& d = g_dev[dev];
+  if (d.ok < 0) {
+    int major = 0, minor = 0, n = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MUON_ERR_CUDA;
+    d.ok = (major == 10 && minor == 3) ? 1 : 0;
+    d.sms = n;
+  }
+  if (d.ok != 1) return MUON_ERR_UNSUPPORTED_DEVICE;
+  sms = d.sms;
+  return MUON_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D bf16 map over `count` matrices of rows x cols (row pitch `pitch`).
+bool encode_map(CUtensorMap* map, void* base, int cols, int rows, int count, int pitch, int box_cols,
+                int box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(count)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch) * 2,
+                           static_cast<cuuint64_t>(pitch) * 2 * static_cast<cuuint64_t>(rows)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sym_tiles_per_mat(int m) {
+  const int tm = static_cast<int>(ceil_div(m, kBM)), tn = static_cast<int>(ceil_div(m, kBN));
+  int t = 0;
+  for (int J = 0; J < tn; ++J) t += std::min(2 * J + 2, tm);
+  return t;
+}
+
+// ------------------------------------------------------------------ the run
+muon_status_t run(const std::vector<JobMat>& mats, const Plan& P, float lr, float mu, int nesterov,
+                  int ns_steps, int final_mode, char* ws, cudaStream_t stream, int sms) {
+  const int N = static_cast<int>(mats.size());
+  int* status = reinterpret_cast<int*>(ws);
+  float* partials = reinterpret_cast<float*>(ws + P.parts_off);
+  MatInfo* table = reinterpret_cast<MatInfo*>(ws + P.table_off);
+  if (cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess) return MUON_ERR_CUDA;
+
+  // momentum + cast (+ transpose) + partial norms
+  for (int k0 = 0; k0 < N; k0 += kK1MaxMats) {
+    K1Params kp;
+    std::memset(&kp, 0, sizeof(kp));
+    const int n = std::min(kK1MaxMats, N - k0);
+    int blocks = 0;
+    for (int j = 0; j < n; ++j) {
+      const int k = k0 + j;
+      const JobMat& M = mats[P.order[k]];
+      int c = 0;
+      while (!(k >= P.cls[c].mat_begin && k < P.cls[c].mat_begin + P.cls[c].count)) ++c;
+      const ClassPlan& cp = P.cls[c];
+      K1Mat& km = kp.mats[j];
+      km.g = M.g;
+      km.buf = M.buf;
+      km.out = M.out;
+      km.x = reinterpret_cast<__nv_bfloat16*>(ws + cp.x_off[0]) +
+             static_cast<long long>(k - cp.mat_begin) * cp.m * cp.ldx;
+      km.R = static_cast<int>(M.R);
+      km.C = static_cast<int>(M.C);
+      km.ldx = cp.ldx;
+      km.tall = M.R > M.C;
+      km.g_f32 = M.g_f32;
+      km.rows_per_block = P.k1_rpb[k];
+      km.part_off = P.part_off[k];
+      km.nparts = P.nparts[k];
+      km.table_index = k;
+      kp.block_begin[j] = blocks;
+      blocks += P.nparts[k];
+    }
+    kp.block_begin[n] = blocks;
+    kp.n = n;
+    kp.mu = mu;
+    kp.nesterov = nesterov;
+    kp.partials = partials;
+    kp.table = table;
+    EventPair ev;
+    const bool rec = ev_begin(ev, 0, stream);
+    if (launch_momentum_cast(kp, blocks, stream) != cudaSuccess) return MUON_ERR_CUDA;
+    ev_end(ev, rec, stream);
+  }
+
+  // normalise (and, for zero steps, the final output)
+  {
+    for (size_t c0 = 0; c0 < P.cls.size(); c0 += kMaxClasses) {
+      NormParams np;
+      std::memset(&np, 0, sizeof(np));
+      const int nc = static_cast<int>(std::min<size_t>(kMaxClasses, P.cls.size() - c0));
+      int blocks = 0;
+      for (int j = 0; j < nc; ++j) {
+        const ClassPlan& cp = P.cls[c0 + j];
+        NormClass& k = np.cls[j];
+        k.x = reinterpret_cast<__nv_bfloat16*>(ws + cp.x_off[0]);
+        k.count = cp.count;
+        k.m = cp.m;
+        k.n = cp.n;
+        k.ldx = cp.ldx;
+        k.mat_begin = cp.mat_begin;
+        k.rows_per_block = cp.norm_rpb;
+        k.blocks_per_mat = cp.norm_blocks;
+        k.block_begin = blocks;
+        blocks += cp.norm_blocks * cp.count;
+      }
+      np.n_classes = nc;
+      np.final_mode = ns_steps == 0 ? final_mode : kFinalNone;
+      np.lr = lr;
+      np.partials = partials;
+      np.table = table;
+      np.status = status;
+      EventPair ev;
+      const bool rec = ev_begin(ev, 1, stream);
+      if (launch_normalise(np, blocks, stream) != cudaSuccess) return MUON_ERR_CUDA;
+      ev_end(ev, rec, stream);
+    }
+  }
+
+  // Newton-Schulz steps
+  const long long budget = g_wait_budget.load();
+  const int stall = g_inject_stall.load();
+  const int store_final = g_store_final_x.load();
+  for (int t = 0; t < ns_steps; ++t) {
+    const int src = t & 1, dst = src ^ 1;
+    const bool last = t == ns_steps - 1;
+    for (size_t c0 = 0; c0 < P.cls.size(); c0 += kMaxClasses) {
+      const int nc = static_cast<int>(std::min<size_t>(kMaxClasses, P.cls.size() - c0));
+      for (int mode = kGram; mode <= kUpdate; ++mode) {
+        GemmParams gp;
+        std::memset(&gp, 0, sizeof(gp));
+        int tiles = 0;
+        for (int j = 0; j < nc; ++j) {
+          const ClassPlan& cp = P.cls[c0 + j];
+          GemmClass& g = gp.cls[j];
+          void* xs = ws + cp.x_off[src];
+          void* xd = ws + cp.x_off[dst];
+          void* A = ws + cp.a_off;
+          void* B = ws + cp.b_off;
+          bool ok = true;
+          if (mode == kGram) {
+            ok = encode_map(&g.tmA, xs, cp.n, cp.m, cp.count, cp.ldx, kBK, kBM) &&
+                 encode_map(&g.tmB, xs, cp.n, cp.m, cp.count, cp.ldx, kBK, kBM);
+            g.out = static_cast<__nv_bfloat16*>(A);
+            g.ld_out = cp.lda;
+            g.out_mat_stride = static_cast<long long>(cp.m) * cp.lda;
+            g.K = cp.n;
+          } else if (mode == kPoly) {
+            ok = encode_map(&g.tmA, A, cp.m, cp.m, cp.count, cp.lda, kBK, kBM) &&
+                 encode_map(&g.tmB, A, cp.m, cp.m, cp.count, cp.lda, kBK, kBM);
+            g.out = static_cast<__nv_bfloat16*>(B);
+            g.ld_out = cp.lda;
+            g.out_mat_stride = static_cast<long long>(cp.m) * cp.lda;
+            g.aux = static_cast<const __nv_bfloat16*>(A);
+            g.ld_aux = cp.lda;
+            g.aux_mat_stride = static_cast<long long>(cp.m) * cp.lda;
+            g.K = cp.m;
+          } else {
+            ok = encode_map(&g.tmA, B, cp.m, cp.m, cp.count, cp.lda, kBK, kBM) &&
+                 encode_map(&g.tmB, xs, cp.n, cp.m, cp.count, cp.ldx, 64, kBK);
+            g.out = static_cast<__nv_bfloat16*>(xd);
+            g.ld_out = cp.ldx;
+            g.out_mat_stride = static_cast<long long>(cp.m) * cp.ldx;
+            g.aux = static_cast<const __nv_bfloat16*>(xs);
+            g.ld_aux = cp.ldx;
+            g.aux_mat_stride = static_cast<long long>(cp.m) * cp.ldx;
+            g.K = cp.m;
+          }
+          if (!ok) return MUON_ERR_CUDA;
+          g.m = cp.m;
+          g.n = cp.n;
+          g.count = cp.count;
+          g.tiles_m = static_cast<int>(ceil_div(cp.m, kBM));
+          if (mode == kUpdate) {
+            g.tiles_n = static_cast<int>(ceil_div(cp.n, kBN));
+            g.tiles_per_mat = g.tiles_m * g.tiles_n;
+          } else {
+            g.tiles_n = static_cast<int>(ceil_div(cp.m, kBN));
+            g.tiles_per_mat = sym_tiles_per_mat(cp.m);
+          }
+          g.tile_begin = tiles;
+          g.mat_begin = cp.mat_begin;
+          tiles += g.tiles_per_mat * cp.count;
+        }
+        gp.n_classes = nc;
+        gp.total_tiles = tiles;
+        gp.ca = kCoefA;
+        gp.cb = kCoefB;
+        gp.cc = kCoefC;
+        gp.final_mode = (mode == kUpdate && last) ? final_mode : kFinalNone;
+        gp.store_x = (mode == kUpdate) && (!last || store_final) ? 1 : 0;
+        gp.lr = lr;
+        gp.table = table;
+        gp.status = status;
+        gp.wait_budget = budget;
+        gp.inject_stall = stall;
+        EventPair ev;
+        const bool rec = ev_begin(ev, 2 + mode, stream);
+        if (launch_ns_gemm(mode, gp, sms, stream) != cudaSuccess) return MUON_ERR_CUDA;
+        ev_end(ev, rec, stream);
+      }
+    }
+  }
+  return MUON_OK;
+}
+
+muon_status_t check_common(int ns_steps, void* ws, size_t ws_bytes, size_t need) {
+  if (ns_steps < 0) return MUON_ERR_INVALID_ARG;
+  if (!ws) return MUON_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return MUON_ERR_MISALIGNED;
+  if (ws_bytes < need) return MUON_ERR_WORKSPACE_TOO_SMALL;
+  return MUON_OK;
+}
+
+muon_status_t plan_and_run(const std::vector<JobMat>& mats, std::vector<Range>& ranges, float lr,
+                           float mu, int nesterov, int ns_steps, int final_mode, void* ws,
+                           size_t ws_bytes, void* stream) {
+  Plan P;
+  if (!build_plan(mats, P)) return MUON_ERR_TOO_LARGE;
+  muon_status_t s = check_common(ns_steps, ws, ws_bytes, P.total);
+  if (s != MUON_OK) return s;
+  ranges.push_back({reinterpret_cast<uintptr_t>(ws), reinterpret_cast<uintptr_t>(ws) + P.total, true});
+  if (ranges_overlap(ranges)) return MUON_ERR_ALIASING;
+  int sms = 0;
+  s = current_device(sms);
+  if (s != MUON_OK) return s;
+  return run(mats, P, lr, mu, nesterov, ns_steps, final_mode, static_cast<char*>(ws),
+             static_cast<cudaStream_t>(stream), sms);
+}
+
+size_t plan_size(const std::vector<JobMat>& mats) {
+  Plan P;
+  if (!build_plan(mats, P)) return 0;
+  return P.total;
+}
+
+bool collect_muon(const muon_mat_desc* mats, int n, std::vector<JobMat>& out,
+                  std::vector<Range>* ranges, muon_status_t& err) {
+  err = MUON_OK;
+  for (int i = 0; i < n; ++i) {
+    const muon_mat_desc& d = mats[i];
+    if (!d.param || !d.grad || !d.buf || d.reserved != 0 ||
+        (d.grad_dtype != MUON_BF16 && d.grad_dtype != MUON_F32)) {
+      err = MUON_ERR_INVALID_ARG;
+      return false;
+    }
+    err = check_shapes(d.rows, d.cols);
+    if (err != MUON_OK) return false;
+    if (!aligned16(d.param) || !aligned16(d.grad) || !aligned16(d.buf)) {
+      err = MUON_ERR_MISALIGNED;
+      return false;
+    }
+    JobMat j;
+    j.g = d.grad;
+    j.g_f32 = d.grad_dtype == MUON_F32;
+    j.buf = d.buf;
+    j.out = d.param;
+    j.R = d.rows;
+    j.C = d.cols;
+    out.push_back(j);
+    if (ranges) {
+      const uintptr_t e = static_cast<uintptr_t>(d.rows * d.cols);
+      const uintptr_t gsz = j.g_f32 ? 4 : 2;
+      ranges->push_back({reinterpret_cast<uintptr_t>(d.param), reinterpret_cast<uintptr_t>(d.param) + 4 * e, true});
+      ranges->push_back({reinterpret_cast<uintptr_t>(d.buf), reinterpret_cast<uintptr_t>(d.buf) + 4 * e, true});
+      ranges->push_back({reinterpret_cast<uintptr_t>(d.grad), reinterpret_cast<uintptr_t>(d.grad) + gsz * e, false});
+    }
+  }
+  return true;
+}
+
+}  // namespace
+}  // namespace muon
+
+using namespace muon;
+
+extern "C" {
+
+size_t muon_workspace_size(const muon_mat_desc* mats, int n_mats) {
+  if (n_mats <= 0 || !mats) return 0;
+  std::vector<JobMat> v;
+  muon_status_t err;
+  // shapes only: pointers may still be unset when sizing
+  for (int i = 0; i < n_mats; ++i) {
+    if (check_shapes(mats[i].rows, mats[i].cols) != MUON_OK) return 0;
+    JobMat j{};
+    j.R = mats[i].rows;
+    j.C = mats[i].cols;
+    v.push_back(j);
+  }
+  (void)err;
+  return plan_size(v);
+}
+
+muon_status_t muon_step(const muon_mat_desc* mats, int n_mats, float lr, float momentum, int nesterov,
+                        int ns_steps, void* workspace, size_t workspace_bytes, void* stream) {
+  if (n_mats == 0) return MUON_OK;
+  if (n_mats < 0 || !mats) return MUON_ERR_INVALID_ARG;
+  if (nesterov != 0 && nesterov != 1) return MUON_ERR_INVALID_ARG;
+  std::vector<JobMat> v;
+  std::vector<Range> ranges;
+  muon_status_t err;
+  if (!collect_muon(mats, n_mats, v, &ranges, err)) return err;
+  return plan_and_run(v, ranges, lr, momentum, nesterov, ns_steps, kFinalParam, workspace,
+                      workspace_bytes, stream);
+}
+
+size_t ns5_workspace_size(int batch, int64_t rows, int64_t cols) {
+  if (batch <= 0 || check_shapes(rows, cols) != MUON_OK) return 0;
+  std::vector<JobMat> v(batch);
+  for (auto& j : v) j.R = rows, j.C = cols;
+  return plan_size(v);
+}
+
+muon_status_t ns5(const void* G, int g_dtype, void* O, int batch, int64_t rows, int64_t cols,
+                  int ns_steps, void* workspace, size_t workspace_bytes, void* stream) {
+  if (batch == 0) return MUON_OK;
+  if (batch < 0 || !G || !O) return MUON_ERR_INVALID_ARG;
+  if (g_dtype != MUON_BF16 && g_dtype != MUON_F32) return MUON_ERR_INVALID_ARG;
+  muon_status_t s = check_shapes(rows, cols);
+  if (s != MUON_OK) return s;
+  if (!aligned16(G) || !aligned16(O)) return MUON_ERR_MISALIGNED;
+  const long long per = rows * cols;
+  const size_t gsz = g_dtype == MUON_F32 ? 4 : 2;
+  std::vector<JobMat> v(batch);
+  for (int i = 0; i < batch; ++i) {
+    v[i].g = static_cast<const char*>(G) + gsz * per * i;
+    v[i].g_f32 = g_dtype == MUON_F32;
+    v[i].buf = nullptr;
+    v[i].out = static_cast<char*>(O) + 2 * per * i;
+    v[i].R = rows;
+    v[i].C = cols;
+  }
+  std::vector<Range> ranges = {
+      {reinterpret_cast<uintptr_t>(G), reinterpret_cast<uintptr_t>(G) + gsz * per * batch, false},
+      {reinterpret_cast<uintptr_t>(O), reinterpret_cast<uintptr_t>(O) + 2 * per * batch, true}};
+  return plan_and_run(v, ranges, 0.0f, 0.0f, 0, ns_steps, kFinalOut, workspace, workspace_bytes, stream);
+}
+
+size_t ns5_bank_workspace_size(const int64_t* rows, const int64_t* cols, int n_mats) {
+  if (n_mats <= 0 || !rows || !cols) return 0;
+  std::vector<JobMat> v(n_mats);
+  for (int i = 0; i < n_mats; ++i) {
+    if (check_shapes(rows[i], cols[i]) != MUON_OK) return 0;
+    v[i].R = rows[i];
+    v[i].C = cols[i];
+  }
+  return plan_size(v);
+}
+
+muon_status_t ns5_bank(const void* const* G, const int32_t* g_dtype, void* const* O, const int64_t* rows,
+                       const int64_t* cols, int n_mats, int ns_steps, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  if (n_mats == 0) return MUON_OK;
+  if (n_mats < 0 || !G || !g_dtype || !O || !rows || !cols) return MUON_ERR_INVALID_ARG;
+  std::vector<JobMat> v(n_mats);
+  std::vector<Range> ranges;
+  for (int i = 0; i < n_mats; ++i) {
+    if (!G[i] || !O[i] || (g_dtype[i] != MUON_BF16 && g_dtype[i] != MUON_F32)) return MUON_ERR_INVALID_ARG;
+    muon_status_t s = check_shapes(rows[i], cols[i]);
+    if (s != MUON_OK) return s;
+    if (!aligned16(G[i]) || !aligned16(O[i])) return MUON_ERR_MISALIGNED;
+    const uintptr_t e = static_cast<uintptr_t>(rows[i] * cols[i]);
+    v[i].g = G[i];
+    v[i].g_f32 = g_dtype[i] == MUON_F32;
+    v[i].buf = nullptr;
+    v[i].out = O[i];
+    v[i].R = rows[i];
+    v[i].C = cols[i];
+    ranges.push_back({reinterpret_cast<uintptr_t>(G[i]),
+                      reinterpret_cast<uintptr_t>(G[i]) + (v[i].g_f32 ? 4 : 2) * e, false});
+    ranges.push_back({reinterpret_cast<uintptr_t>(O[i]), reinterpret_cast<uintptr_t>(O[i]) + 2 * e, true});
+  }
+  return plan_and_run(v, ranges, 0.0f, 0.0f, 0, ns_steps, kFinalOut, workspace, workspace_bytes, stream);
+}
+
+muon_status_t muon_device_status(const void* workspace, void* stream) {
+  if (!workspace) return MUON_ERR_INVALID_ARG;
+  int v = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MUON_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MUON_ERR_CUDA;
+  if (v & kStatusTimeout) return MUON_ERR_DEVICE_TIMEOUT;
+  if (v & kStatusNonFinite) return MUON_WARN_NONFINITE;
+  return MUON_OK;
+}
+
+const char* muon_status_str(muon_status_t s) {
+  switch (s) {
+    case MUON_OK: return "ok";
+    case MUON_WARN_NONFINITE: return "warning: a matrix had a non-finite norm";
+    case MUON_ERR_INVALID_ARG: return "invalid argument";
+    case MUON_ERR_MISALIGNED: return "pointer not 16-byte aligned (workspace: 256-byte)";
+    case MUON_ERR_ALIASING: return "operands overlap";
+    case MUON_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MUON_ERR_CUDA: return "CUDA runtime error";
+    case MUON_ERR_DEVICE_TIMEOUT: return "bounded device wait expired";
+    case MUON_ERR_UNSUPPORTED_DEVICE: return "current device is not compute capability 10.3 (sm_103)";
+    case MUON_ERR_TOO_LARGE: return "dimension too large";
+  }
+  return "unknown status";
+}
+
+muon_status_t ns5_workspace_layout(int batch, int64_t rows, int64_t cols, muon_ws_layout* out) {
+  if (!out || batch <= 0) return MUON_ERR_INVALID_ARG;
+  muon_status_t s = check_shapes(rows, cols);
+  if (s != MUON_OK) return s;
+  std::vector<JobMat> v(batch);
+  for (auto& j : v) j.R = rows, j.C = cols;
+  Plan P;
+  if (!build_plan(v, P)) return MUON_ERR_TOO_LARGE;
+  const ClassPlan& c = P.cls[0];
+  out->x_offset[0] = c.x_off[0];
+  out->x_offset[1] = c.x_off[1];
+  out->a_offset = c.a_off;
+  out->b_offset = c.b_off;
+  out->ldx = c.ldx;
+  out->lda = c.lda;
+  out->m = c.m;
+  out->n = c.n;
+  return MUON_OK;
+}
+
+int muon_set_debug(const char* key, long long value) {
+  if (!key) return -1;
+  if (!std::strcmp(key, "wait_budget_cycles")) {
+    g_wait_budget.store(value > 0 ? value : 1);
+    return 0;
+  }
+  if (!std::strcmp(key, "inject_stall")) {
+    g_inject_stall.store(value ? 1 : 0);
+    return 0;
+  }
+  if (!std::strcmp(key, "record_kernel_events")) {
+    g_record_events.store(value ? 1 : 0);
+    return 0;
+  }
+  if (!std::strcmp(key, "store_final_x")) {
+    g_store_final_x.store(value ? 1 : 0);
+    return 0;
+  }
+  return -1;
+}
+
+int muon_kernel_times(double* ms, int* launches, int n_kinds) {
+  if (!ms || !launches || n_kinds <= 0) return -1;
+  for (int k = 0; k < n_kinds; ++k) ms[k] = 0.0, launches[k] = 0;
+  std::vector<EventPair> pending;
+  {
+    std::lock_guard<std::mutex> lk(g_ev_mu);
+    pending.swap(g_ev_pending);
+  }
+  int rc = 0;
+  for (EventPair& e : pending) {
+    float t = 0.0f;
+    if (cudaEventSynchronize(e.stop) != cudaSuccess || cudaEventElapsedTime(&t, e.start, e.stop) != cudaSuccess)
+      rc = -1;
+    if (e.kind < n_kinds) {
+      ms[e.kind] += t;
+      launches[e.kind] += 1;
+    }
+  }
+  std::lock_guard<std::mutex> lk(g_ev_mu);
+  g_ev_pool.insert(g_ev_pool.end(), pending.begin(), pending.end());
+  return rc;
+}
+
+}  // extern "C"

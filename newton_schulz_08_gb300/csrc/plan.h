@@ -1,0 +1,127 @@
+// Internal launch-parameter structures shared by the host planner
+// (muon_capi.cu) and the kernels (elementwise.cu, ns_gemm.cu).
+//
+// A bank of matrices is grouped into shape classes (m, n) with m = min(R, C)
+// and n = max(R, C): after the momentum pass every matrix of a class is held
+// in the workspace as X (m x n, bf16, row-major, row pitch ldx), tall matrices
+// already transposed.  The Newton-Schulz kernels iterate over all tiles of
+// all classes in one persistent launch per phase.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace muon {
+
+constexpr int kMaxClasses = 8;     // shape classes per launch
+constexpr int kK1MaxMats = 96;     // matrices per momentum-pass launch
+
+// device status word bits (kept in the workspace header)
+constexpr int kStatusNonFinite = 1;
+constexpr int kStatusTimeout = 2;
+
+enum GemmMode { kGram = 0, kPoly = 1, kUpdate = 2 };
+enum FinalMode { kFinalNone = 0, kFinalParam = 1, kFinalOut = 2 };
+
+// One row per matrix of the bank; written by the momentum pass into the
+// workspace, read by the normalise pass and the last B*X launch.
+struct MatInfo {
+  void* out;        // fp32 param (Muon step) or bf16 O (Newton-Schulz only)
+  int R, C;         // stored shape
+  int tall;         // R > C: X = u^T
+  int part_off;     // first partial sum of this matrix
+  int nparts;       // number of partial sums
+  int pad;
+};
+
+// ---------------------------------------------------------------- momentum
+struct K1Mat {
+  const void* g;      // gradient (or G), R x C, row-major
+  float* buf;         // momentum buffer (null: no momentum, u = g)
+  void* out;          // recorded in MatInfo
+  __nv_bfloat16* x;   // X destination in the workspace
+  int R, C, ldx;
+  int tall;
+  int g_f32;          // 1: g is float32, 0: bfloat16
+  int rows_per_block; // wide: rows per block; tall: 64
+  int part_off;       // first partial of this matrix
+  int nparts;
+  int table_index;    // global matrix index in the MatInfo table
+  int pad;
+};
+
+struct K1Params {
+  K1Mat mats[kK1MaxMats];
+  int block_begin[kK1MaxMats + 1];
+  int n;
+  float mu;
+  int nesterov;
+  float* partials;
+  MatInfo* table;
+};
+
+// ---------------------------------------------------------------- normalise
+struct NormClass {
+  __nv_bfloat16* x;   // class region, count x m x ldx
+  int count, m, n, ldx;
+  int mat_begin;      // first global matrix index of the class
+  int rows_per_block;
+  int blocks_per_mat;
+  int block_begin;
+};
+
+struct NormParams {
+  NormClass cls[kMaxClasses];
+  int n_classes;
+  int final_mode;     // ns_steps == 0: write O / update p here
+  float lr;
+  const float* partials;
+  const MatInfo* table;
+  int* status;
+};
+
+// ---------------------------------------------------------------- GEMMs
+struct GemmClass {
+  CUtensorMap tmA;              // operand A (K-major rows, box 64 x 128)
+  CUtensorMap tmB;              // operand B (Gram/poly: K-major box 64 x 128;
+                                //            update: MN-major box 64 x 64)
+  __nv_bfloat16* out;           // output region (A, B or X_{t+1})
+  const __nv_bfloat16* aux;     // epilogue input (A for poly, X_t for update)
+  long long out_mat_stride;     // elements between matrices of out
+  long long aux_mat_stride;
+  int ld_out, ld_aux;
+  int m, n, count, K;
+  int tiles_m, tiles_n, tiles_per_mat;
+  int tile_begin;
+  int mat_begin;
+  int pad[3];
+};
+
+struct GemmParams {
+  GemmClass cls[kMaxClasses];
+  int n_classes;
+  int total_tiles;
+  float ca, cb, cc;             // Newton-Schulz coefficients
+  int final_mode;
+  int store_x;                  // update: also store X_{t+1}
+  float lr;
+  const MatInfo* table;
+  int* status;
+  long long wait_budget;        // clock64 cycles per barrier wait
+  int inject_stall;             // test hook: MMA warp issues nothing
+  int pad;
+};
+
+// tile sizes of the tcgen05 kernels
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kStageA = kBM * kBK * 2;        // 16 KB
+constexpr int kStageB = kBN * kBK * 2;        // 32 KB
+constexpr int kStageBytes = kStageA + kStageB;
+constexpr int kGemmSmem = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int kGemmThreads = 192;
+
+}  // namespace muon

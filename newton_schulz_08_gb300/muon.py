@@ -1,0 +1,244 @@
+"""ctypes binding of libmuon.so (include/muon.h): argument marshalling only.
+
+Every step of the Muon update runs inside the library's CUDA kernels; this
+module turns torch tensors into device pointers and the current torch stream
+into a cudaStream_t, allocates the workspace with torch when the caller does
+not pass one, and raises ``MuonError`` on a non-OK status.  It loads the
+library on first use and fails loudly if it has not been built.
+"""
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libmuon.so")
+
+MUON_OK = 0
+MUON_WARN_NONFINITE = 1
+MUON_ERR_INVALID_ARG = -1
+MUON_ERR_MISALIGNED = -2
+MUON_ERR_ALIASING = -3
+MUON_ERR_WORKSPACE_TOO_SMALL = -4
+MUON_ERR_CUDA = -5
+MUON_ERR_DEVICE_TIMEOUT = -6
+MUON_ERR_UNSUPPORTED_DEVICE = -7
+MUON_ERR_TOO_LARGE = -8
+MUON_BF16 = 0
+MUON_F32 = 1
+
+#: every symbol include/muon.h declares
+EXPORTS = ["muon_workspace_size", "muon_step", "ns5_workspace_size", "ns5", "ns5_bank",
+           "ns5_bank_workspace_size", "muon_device_status", "muon_status_str",
+           "ns5_workspace_layout", "muon_set_debug", "muon_kernel_times"]
+
+#: kernel kinds reported by muon_kernel_times
+KERNEL_KINDS = ["momentum_cast", "normalise", "gram", "poly", "update"]
+
+
+class MuonError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {muon_status_str(status)} (status {status})")
+
+
+class muon_mat_desc(ctypes.Structure):
+    _fields_ = [("param", ctypes.c_void_p), ("grad", ctypes.c_void_p), ("buf", ctypes.c_void_p),
+                ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("grad_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class muon_ws_layout(ctypes.Structure):
+    _fields_ = [("x_offset", ctypes.c_size_t * 2), ("a_offset", ctypes.c_size_t),
+                ("b_offset", ctypes.c_size_t), ("ldx", ctypes.c_int64), ("lda", ctypes.c_int64),
+                ("m", ctypes.c_int64), ("n", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "`python -m newton_schulz_08_gb300.build` (or __graft_entry__.build())")
+    L = ctypes.CDLL(LIB_PATH)
+    c_int, c_i64, c_sz, c_vp, c_f = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
+    P = ctypes.POINTER
+    L.muon_workspace_size.argtypes = [P(muon_mat_desc), c_int]
+    L.muon_workspace_size.restype = c_sz
+    L.muon_step.argtypes = [P(muon_mat_desc), c_int, c_f, c_f, c_int, c_int, c_vp, c_sz, c_vp]
+    L.muon_step.restype = c_int
+    L.ns5_workspace_size.argtypes = [c_int, c_i64, c_i64]
+    L.ns5_workspace_size.restype = c_sz
+    L.ns5.argtypes = [c_vp, c_int, c_vp, c_int, c_i64, c_i64, c_int, c_vp, c_sz, c_vp]
+    L.ns5.restype = c_int
+    L.ns5_bank.argtypes = [P(c_vp), P(ctypes.c_int32), P(c_vp), P(c_i64), P(c_i64), c_int, c_int,
+                           c_vp, c_sz, c_vp]
+    L.ns5_bank.restype = c_int
+    L.ns5_bank_workspace_size.argtypes = [P(c_i64), P(c_i64), c_int]
+    L.ns5_bank_workspace_size.restype = c_sz
+    L.muon_device_status.argtypes = [c_vp, c_vp]
+    L.muon_device_status.restype = c_int
+    L.muon_status_str.argtypes = [c_int]
+    L.muon_status_str.restype = ctypes.c_char_p
+    L.ns5_workspace_layout.argtypes = [c_int, c_i64, c_i64, P(muon_ws_layout)]
+    L.ns5_workspace_layout.restype = c_int
+    L.muon_set_debug.argtypes = [ctypes.c_char_p, ctypes.c_longlong]
+    L.muon_set_debug.restype = c_int
+    L.muon_kernel_times.argtypes = [P(ctypes.c_double), P(c_int), c_int]
+    L.muon_kernel_times.restype = c_int
+    _lib = L
+    return L
+
+
+def muon_status_str(status):
+    return lib().muon_status_str(int(status)).decode()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(status, where, ok=(MUON_OK,)):
+    if status not in ok:
+        raise MuonError(status, where)
+    return status
+
+
+def _dtype_code(t):
+    if t.dtype == torch.bfloat16:
+        return MUON_BF16
+    if t.dtype == torch.float32:
+        return MUON_F32
+    raise TypeError(f"unsupported dtype {t.dtype} (bfloat16 or float32)")
+
+
+def _descs(params, grads, bufs):
+    n = len(params)
+    if len(grads) != n or len(bufs) != n:
+        raise ValueError("params, grads and bufs must have the same length")
+    arr = (muon_mat_desc * max(n, 1))()
+    for i, (p, g, b) in enumerate(zip(params, grads, bufs)):
+        if p.dim() != 2 or g.shape != p.shape or b.shape != p.shape:
+            raise ValueError(f"matrix {i}: param, grad and buf must be 2-D of one shape")
+        if p.dtype != torch.float32 or b.dtype != torch.float32:
+            raise TypeError(f"matrix {i}: param and buf must be float32")
+        if not (p.is_contiguous() and g.is_contiguous() and b.is_contiguous()):
+            raise ValueError(f"matrix {i}: tensors must be contiguous")
+        arr[i] = muon_mat_desc(p.data_ptr(), g.data_ptr(), b.data_ptr(), p.shape[0], p.shape[1],
+                               _dtype_code(g), 0)
+    return arr, n
+
+
+def muon_workspace_size(shapes):
+    """Workspace bytes for a bank given as a list of (rows, cols)."""
+    n = len(shapes)
+    arr = (muon_mat_desc * max(n, 1))()
+    for i, (r, c) in enumerate(shapes):
+        arr[i] = muon_mat_desc(0, 0, 0, r, c, MUON_BF16, 0)
+    return lib().muon_workspace_size(arr, n)
+
+
+def new_workspace(nbytes, device=None):
+    device = device or torch.device("cuda", torch.cuda.current_device())
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def muon_step(params, grads, bufs, lr=0.02, momentum=0.95, nesterov=True, ns_steps=5,
+              workspace=None, stream=None):
+    """One Muon step over a bank (lists of 2-D CUDA tensors), in place."""
+    arr, n = _descs(params, grads, bufs)
+    if workspace is None:
+        workspace = new_workspace(lib().muon_workspace_size(arr, n), params[0].device)
+    st = lib().muon_step(arr, n, float(lr), float(momentum), int(bool(nesterov)), int(ns_steps),
+                         ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream(stream))
+    _check(st, "muon_step")
+    return workspace
+
+
+def ns5_workspace_size(batch, rows, cols):
+    return lib().ns5_workspace_size(int(batch), int(rows), int(cols))
+
+
+def ns5(G, ns_steps=5, out=None, workspace=None, stream=None):
+    """zeropower_via_newtonschulz5 on a (batch x) rows x cols CUDA tensor -> bf16."""
+    squeeze = G.dim() == 2
+    G3 = G.unsqueeze(0) if squeeze else G
+    if G3.dim() != 3 or not G3.is_contiguous():
+        raise ValueError("G must be a contiguous 2-D or 3-D tensor")
+    batch, rows, cols = G3.shape
+    if out is None:
+        out = torch.empty(G3.shape, dtype=torch.bfloat16, device=G.device)
+    if out.shape != G3.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bfloat16 tensor shaped like G")
+    if workspace is None:
+        workspace = new_workspace(ns5_workspace_size(batch, rows, cols) if batch else 256, G.device)
+    st = lib().ns5(ctypes.c_void_p(G3.data_ptr()), _dtype_code(G3), ctypes.c_void_p(out.data_ptr()),
+                   batch, rows, cols, int(ns_steps), ctypes.c_void_p(workspace.data_ptr()),
+                   workspace.numel(), _stream(stream))
+    _check(st, "ns5")
+    return out[0] if squeeze else out
+
+
+def ns5_bank_workspace_size(shapes):
+    n = len(shapes)
+    rows = (ctypes.c_int64 * max(n, 1))(*[s[0] for s in shapes])
+    cols = (ctypes.c_int64 * max(n, 1))(*[s[1] for s in shapes])
+    return lib().ns5_bank_workspace_size(rows, cols, n)
+
+
+def ns5_bank(Gs, ns_steps=5, outs=None, workspace=None, stream=None):
+    """Newton-Schulz on a list of differently shaped 2-D CUDA tensors -> bf16 list."""
+    n = len(Gs)
+    if outs is None:
+        outs = [torch.empty(g.shape, dtype=torch.bfloat16, device=g.device) for g in Gs]
+    gp = (ctypes.c_void_p * max(n, 1))(*[g.data_ptr() for g in Gs])
+    op = (ctypes.c_void_p * max(n, 1))(*[o.data_ptr() for o in outs])
+    dt = (ctypes.c_int32 * max(n, 1))(*[_dtype_code(g) for g in Gs])
+    rows = (ctypes.c_int64 * max(n, 1))(*[g.shape[0] for g in Gs])
+    cols = (ctypes.c_int64 * max(n, 1))(*[g.shape[1] for g in Gs])
+    for g, o in zip(Gs, outs):
+        if g.dim() != 2 or not g.is_contiguous() or o.shape != g.shape or o.dtype != torch.bfloat16:
+            raise ValueError("each G must be 2-D contiguous with a bf16 out of the same shape")
+    if workspace is None:
+        workspace = new_workspace(lib().ns5_bank_workspace_size(rows, cols, n) if n else 256,
+                                  Gs[0].device if n else None)
+    st = lib().ns5_bank(gp, dt, op, rows, cols, n, int(ns_steps),
+                        ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream(stream))
+    _check(st, "ns5_bank")
+    return outs
+
+
+def muon_device_status(workspace, stream=None):
+    """Synchronise and read the workspace's device status word (an int code)."""
+    return lib().muon_device_status(ctypes.c_void_p(workspace.data_ptr()), _stream(stream))
+
+
+def ns5_workspace_layout(batch, rows, cols):
+    out = muon_ws_layout()
+    _check(lib().ns5_workspace_layout(int(batch), int(rows), int(cols), ctypes.byref(out)),
+           "ns5_workspace_layout")
+    return {"x_offset": (out.x_offset[0], out.x_offset[1]), "a_offset": out.a_offset,
+            "b_offset": out.b_offset, "ldx": out.ldx, "lda": out.lda, "m": out.m, "n": out.n}
+
+
+def muon_set_debug(key, value):
+    if lib().muon_set_debug(key.encode(), int(value)) != 0:
+        raise KeyError(key)
+
+
+def muon_kernel_times():
+    """{kind: (total_ms, launches)} for launches recorded since the last call."""
+    n = len(KERNEL_KINDS)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int * n)()
+    if lib().muon_kernel_times(ms, cnt, n) != 0:
+        raise RuntimeError("muon_kernel_times failed")
+    return {k: (ms[i], cnt[i]) for i, k in enumerate(KERNEL_KINDS)}

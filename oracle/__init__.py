@@ -30,7 +30,11 @@ from .muon import (
     momentum_update,
     orient,
     normalise,
+    ns_gram,
+    ns_poly,
+    ns_update,
     ns_iteration,
+    ns_iteration_parts,
     newton_schulz5,
     muon_step,
 )
@@ -44,7 +48,11 @@ __all__ = [
     "momentum_update",
     "orient",
     "normalise",
+    "ns_gram",
+    "ns_poly",
+    "ns_update",
     "ns_iteration",
+    "ns_iteration_parts",
     "newton_schulz5",
     "muon_step",
 ]

@@ -88,16 +88,39 @@ def normalise(G, mode="fp64"):
     return round_to_bf16(Xb / (nu + NORM_EPS))
 
 
+def ns_gram(X, mode="fp64"):
+    """A = X X^T (rounded to bfloat16 in bf16 mode)."""
+    A = X @ X.T
+    return A if mode == "fp64" else round_to_bf16(A)
+
+
+def ns_poly(A, mode="fp64"):
+    """B = b A + c A A (one rounding in bf16 mode)."""
+    _, b, c = _coeffs(mode)
+    B = b * A + c * (A @ A)
+    return B if mode == "fp64" else round_to_bf16(B)
+
+
+def ns_update(B, X, mode="fp64"):
+    """X' = a X + B X (one rounding in bf16 mode)."""
+    a = _coeffs(mode)[0]
+    Xn = a * X + B @ X
+    return Xn if mode == "fp64" else round_to_bf16(Xn)
+
+
+def ns_iteration_parts(X, mode="fp64"):
+    """One quintic step: A = X X^T; B = b A + c A A; X' = a X + B X.
+
+    Returns (A, B, X') so that tests can look at the intermediate matrices.
+    """
+    A = ns_gram(X, mode)
+    B = ns_poly(A, mode)
+    return A, B, ns_update(B, X, mode)
+
+
 def ns_iteration(X, mode="fp64"):
-    """One quintic step: A = X X^T; B = b A + c A A; X' = a X + B X."""
-    a, b, c = _coeffs(mode)
-    if mode == "fp64":
-        A = X @ X.T
-        B = b * A + c * (A @ A)
-        return a * X + B @ X
-    A = round_to_bf16(X @ X.T)
-    B = round_to_bf16(b * A + c * (A @ A))
-    return round_to_bf16(a * X + B @ X)
+    """One quintic step; returns X'."""
+    return ns_iteration_parts(X, mode)[2]
 
 
 def newton_schulz5(G, steps=5, mode="fp64"):

@@ -1,0 +1,247 @@
+"""GPU parity of each kernel and of small end-to-end calls, through the C ABI.
+
+Every comparison is against the CPU oracle on the same seeded inputs.  The
+single-step test isolates each tensor-core kernel: the oracle's step function
+is fed the GPU's own input to that kernel (X0 for the Gram, A for the
+polynomial, B and X0 for the update), so a mismatch points at one kernel.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from newton_schulz_08_gb300 import muon
+from tests.gpu_helpers import (TOL_BUF_REL, TOL_MAXABS_BF16, TOL_REL_BF16, TOL_REL_FP64,
+                               assert_bf16_close, bf16_np, check_status, rel, to_dev, ws_view)
+
+pytestmark = pytest.mark.gpu
+
+A_, B_, C_ = (float(np.float32(v)) for v in oracle.NS_COEFFS)
+
+# spans one tile, several tiles, ragged tails in both dimensions, tall and
+# wide, columns that are not a multiple of 8, and degenerate 1-wide shapes
+SHAPES = [(128, 512), (256, 256), (200, 328), (300, 100), (129, 257), (100, 37), (37, 100),
+          (1, 1), (1, 37), (37, 1), (384, 1536), (1536, 384), (520, 520)]
+
+
+def gauss(shape, seed, scale=1.0):
+    return (np.random.default_rng(seed).standard_normal(shape) * scale).astype(np.float32)
+
+
+def as_seen(G, dtype):
+    """The values the GPU reads: bf16 inputs are rounded on upload."""
+    return oracle.round_to_bf16(G) if dtype == torch.bfloat16 else G.astype(np.float64)
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_normalise_x0(shape, dtype):
+    G = gauss(shape, 1)
+    out = muon.ns5(to_dev(G, dtype), ns_steps=0)
+    torch.cuda.synchronize()
+    want = oracle.newton_schulz5(as_seen(G, dtype), 0, "bf16")
+    assert_bf16_close(bf16_np(out), want, 0.0, "X0", slack=0.0, max_frac=2e-3)
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_one_step_each_kernel(shape):
+    R, C = shape
+    G = gauss(shape, 2)
+    lay = muon.ns5_workspace_layout(1, R, C)
+    ws = muon.new_workspace(muon.ns5_workspace_size(1, R, C))
+    muon.muon_set_debug("store_final_x", 1)
+    try:
+        out = muon.ns5(to_dev(G), ns_steps=1, workspace=ws)
+        check_status(ws)
+    finally:
+        muon.muon_set_debug("store_final_x", 0)
+    m, n, ldx, lda = lay["m"], lay["n"], lay["ldx"], lay["lda"]
+    X0 = ws_view(ws, lay["x_offset"][0], m, n, ldx)
+    A = ws_view(ws, lay["a_offset"], m, m, lda)
+    B = ws_view(ws, lay["b_offset"], m, m, lda)
+    X1 = ws_view(ws, lay["x_offset"][1], m, n, ldx)
+    # X0 is the oracle's normalised input (orientation: tall inputs transposed)
+    Gv, tall = oracle.orient(G.astype(np.float64))
+    assert_bf16_close(X0, oracle.normalise(Gv, "bf16"), 0.0, "X0", slack=0.0, max_frac=2e-3)
+    # Gram kernel: exactly symmetric, A = bf16(X0 X0^T)
+    assert np.array_equal(A, A.T)
+    absX = np.abs(X0)
+    assert_bf16_close(A, oracle.ns_gram(X0, "bf16"), absX @ absX.T, "A")
+    # polynomial kernel: symmetric, B = bf16(b A + c A A)
+    assert np.array_equal(B, B.T)
+    absA = np.abs(A)
+    assert_bf16_close(B, oracle.ns_poly(A, "bf16"), abs(B_) * absA + abs(C_) * absA @ absA, "B")
+    # update kernel: X1 = bf16(a X0 + B X0), and O is X1 in G's orientation
+    assert_bf16_close(X1, oracle.ns_update(B, X0, "bf16"), abs(A_) * absX + np.abs(B) @ absX, "X1")
+    O = bf16_np(out)
+    assert np.array_equal(O, X1.T if tall else X1)
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("steps", [2, 5])
+def test_ns5_matches_oracle(shape, steps):
+    G = gauss(shape, 3)
+    out = bf16_np(muon.ns5(to_dev(G), ns_steps=steps))
+    ob = oracle.newton_schulz5(G, steps, "bf16")
+    of = oracle.newton_schulz5(G, steps, "fp64")
+    if min(shape) == 1:
+        # a single row or column: O = p^steps(~1) g/||g||, exact up to rounding
+        assert np.abs(out - ob).max() <= 2 * bf16_ulp_max(ob)
+        return
+    assert rel(out, ob) <= TOL_REL_BF16
+    assert np.abs(out - ob).max() <= TOL_MAXABS_BF16
+    assert rel(out, of) <= TOL_REL_FP64
+
+
+def bf16_ulp_max(v):
+    from tests.gpu_helpers import bf16_ulp
+    return float(bf16_ulp(np.abs(v).max()))
+
+
+def test_ns5_batched_equals_single():
+    G = gauss((5, 200, 328), 4)
+    Gt = to_dev(G)
+    batched = muon.ns5(Gt, 5)
+    for i in range(5):
+        single = muon.ns5(Gt[i].contiguous(), 5)
+        assert torch.equal(batched[i], single)
+
+
+def test_ns5_bank_equals_per_shape_calls():
+    shapes = [(200, 328), (328, 200), (64, 64), (128, 512), (37, 100)]
+    Gs = [to_dev(gauss(s, 10 + i)) for i, s in enumerate(shapes)]
+    outs = muon.ns5_bank(Gs, 5)
+    for g, o in zip(Gs, outs):
+        assert torch.equal(o, muon.ns5(g, 5))
+
+
+def run_step(shapes, nesterov=True, steps=5, gdtype=torch.bfloat16, seed=0, lr=0.02, mu=0.95):
+    rng = np.random.default_rng(seed)
+    ps = [rng.standard_normal(s).astype(np.float32) * np.float32(0.02) for s in shapes]
+    gs = [rng.standard_normal(s).astype(np.float32) * np.float32(1e-3) for s in shapes]
+    bs = [rng.standard_normal(s).astype(np.float32) * np.float32(1e-3) for s in shapes]
+    P = [to_dev(p) for p in ps]
+    Gd = [to_dev(g, gdtype) for g in gs]
+    Bd = [to_dev(b) for b in bs]
+    ws = muon.muon_step(P, Gd, Bd, lr=lr, momentum=mu, nesterov=nesterov, ns_steps=steps)
+    check_status(ws)
+    gseen = [as_seen(g, gdtype).astype(np.float32) for g in gs]
+    return ps, gseen, bs, [t.cpu().numpy() for t in P], [t.cpu().numpy() for t in Bd]
+
+
+@pytest.mark.parametrize("nesterov", [True, False])
+@pytest.mark.parametrize("gdtype", [torch.bfloat16, torch.float32])
+def test_muon_step_mixed_bank(nesterov, gdtype):
+    shapes = [(256, 256), (300, 100), (100, 300), (129, 257), (64, 64), (37, 100), (256, 256)]
+    lr, mu = 0.02, 0.95
+    ps, gs, bs, P, Bn = run_step(shapes, nesterov, 5, gdtype, seed=5, lr=lr, mu=mu)
+    for i in range(len(shapes)):
+        new_p, new_buf, O = oracle.muon_step(ps[i], gs[i], bs[i], lr, mu, nesterov, 5, "bf16")
+        assert rel(Bn[i], new_buf) <= TOL_BUF_REL
+        O_gpu = (ps[i].astype(np.float64) - P[i].astype(np.float64)) / lr
+        assert rel(O_gpu, O) <= TOL_REL_BF16, i
+        assert np.abs(O_gpu - O).max() <= TOL_MAXABS_BF16
+        _, _, O64 = oracle.muon_step(ps[i], gs[i], bs[i], lr, mu, nesterov, 5, "fp64")
+        assert rel(O_gpu, O64) <= TOL_REL_FP64
+
+
+def test_param_update_is_exact_given_gpu_O():
+    """p_new = p - lr * O_gpu in fp32, O_gpu read from the workspace."""
+    R, C = 300, 100
+    rng = np.random.default_rng(6)
+    p = (rng.standard_normal((R, C)) * 0.02).astype(np.float32)
+    g = rng.standard_normal((R, C)).astype(np.float32)
+    b = np.zeros((R, C), np.float32)
+    P, Gd, Bd = to_dev(p), to_dev(g), to_dev(b)
+    lay = muon.ns5_workspace_layout(1, R, C)
+    ws = muon.new_workspace(muon.muon_workspace_size([(R, C)]))
+    muon.muon_set_debug("store_final_x", 1)
+    try:
+        muon.muon_step([P], [Gd], [Bd], lr=0.02, momentum=0.95, ns_steps=5, workspace=ws)
+        check_status(ws)
+    finally:
+        muon.muon_set_debug("store_final_x", 0)
+    X5 = ws_view(ws, lay["x_offset"][1], lay["m"], lay["n"], lay["ldx"])  # 5 steps end in buffer 1
+    O = X5.T  # tall
+    want = (p - np.float32(0.02) * O.astype(np.float32)).astype(np.float32)
+    got = P.cpu().numpy()
+    assert np.abs(got - want).max() <= 1e-5 * np.abs(want).max()
+    assert rel(got, want) <= 1e-5
+
+
+def test_zero_matrix_leaves_param():
+    p = np.random.default_rng(7).standard_normal((128, 256)).astype(np.float32)
+    P = to_dev(p)
+    z = torch.zeros((128, 256), device="cuda", dtype=torch.bfloat16)
+    b = torch.zeros((128, 256), device="cuda")
+    ws = muon.muon_step([P], [z], [b])
+    check_status(ws)
+    assert np.array_equal(P.cpu().numpy(), p)
+
+
+def test_nonfinite_is_reported():
+    G = gauss((64, 128), 8)
+    G[3, 5] = np.inf
+    ws = muon.new_workspace(muon.ns5_workspace_size(1, 64, 128))
+    muon.ns5(to_dev(G), 5, workspace=ws)
+    assert muon.muon_device_status(ws) == muon.MUON_WARN_NONFINITE
+    # a finite call on the same workspace clears the status
+    muon.ns5(to_dev(gauss((64, 128), 9)), 5, workspace=ws)
+    assert muon.muon_device_status(ws) == muon.MUON_OK
+
+
+def test_bounded_wait_expires_and_context_survives():
+    G = to_dev(gauss((256, 512), 11))
+    ws = muon.new_workspace(muon.ns5_workspace_size(1, 256, 512))
+    muon.muon_set_debug("inject_stall", 1)
+    muon.muon_set_debug("wait_budget_cycles", 20_000_000)  # ~10 ms
+    try:
+        muon.ns5(G, 1, workspace=ws)
+        st = muon.muon_device_status(ws)
+    finally:
+        muon.muon_set_debug("inject_stall", 0)
+        muon.muon_set_debug("wait_budget_cycles", 4_000_000_000)
+    assert st == muon.MUON_ERR_DEVICE_TIMEOUT
+    out = muon.ns5(G, 5, workspace=ws)
+    check_status(ws)
+    ob = oracle.newton_schulz5(G.cpu().numpy(), 5, "bf16")
+    assert rel(bf16_np(out), ob) <= TOL_REL_BF16
+
+
+def test_deterministic():
+    shapes = [(256, 256), (300, 100)]
+    r1 = run_step(shapes, seed=12)
+    r2 = run_step(shapes, seed=12)
+    for a, b in zip(r1[3] + r1[4], r2[3] + r2[4]):
+        assert np.array_equal(a, b)
+
+
+def test_resume_matches_straight_run():
+    """3 steps in a row == 2 steps, state copied to the host and back, 1 step."""
+    shapes = [(200, 328), (328, 200)]
+    rng = np.random.default_rng(13)
+    p0 = [(rng.standard_normal(s) * 0.02).astype(np.float32) for s in shapes]
+    grads = [[to_dev(rng.standard_normal(s).astype(np.float32) * 1e-3, torch.bfloat16) for s in shapes]
+             for _ in range(3)]
+
+    def fresh():
+        return [to_dev(p) for p in p0], [torch.zeros(s, device="cuda") for s in shapes]
+
+    P1, B1 = fresh()
+    for k in range(3):
+        muon.muon_step(P1, grads[k], B1)
+    P2, B2 = fresh()
+    for k in range(2):
+        muon.muon_step(P2, grads[k], B2)
+    host = [t.cpu() for t in P2 + B2]
+    P3 = [h.cuda() for h in host[:2]]
+    B3 = [h.cuda() for h in host[2:]]
+    muon.muon_step(P3, grads[2], B3)
+    for a, b in zip(P1 + B1, P3 + B3):
+        assert torch.equal(a, b)
+
+
+def test_empty_calls():
+    assert muon.ns5(torch.empty((0, 8, 8), device="cuda"), 5).shape == (0, 8, 8)
+    assert muon.ns5_bank([], 5) == []

@@ -228,19 +228,14 @@ def test_muon_step_tall_orientation():
 
 
 # ------------------------------------------------------------- planted mistakes
-def _wrong_update(X, mode="fp64"):
-    a, b, c = om._coeffs(mode)
-    A = X @ X.T
-    B = b * A + c * (A @ A)
-    return a * X + X @ B  # transposed operand order
+def _coeffs_a(mode):
+    return om._coeffs(mode)[0]
 
 
-def _double_round_poly(X, mode="fp64"):
-    a, b, c = om._coeffs(mode)
-    A = oracle.round_to_bf16(X @ X.T)
+def _double_round_poly(A):
+    _, b, c = om._coeffs("bf16")
     AA = oracle.round_to_bf16(A @ A)  # extra rounding of A A
-    B = oracle.round_to_bf16(b * A + c * AA)
-    return oracle.round_to_bf16(a * X + B @ X)
+    return oracle.round_to_bf16(b * A + c * AA)
 
 
 def _eps_on_square(G, mode="fp64"):
@@ -282,13 +277,13 @@ def test_planted_mistakes_are_caught(monkeypatch, mistake):
     elif mistake == "drop_c":
         monkeypatch.setattr(om, "NS_COEFFS", (COEFFS[0], COEFFS[1], 0.0))
     elif mistake == "update_order":
-        monkeypatch.setattr(om, "ns_iteration", _wrong_update)
+        monkeypatch.setattr(om, "ns_update", lambda B, X, mode="fp64": _coeffs_a(mode) * X + X @ B)
     elif mistake == "eps_on_square":
         monkeypatch.setattr(om, "normalise", _eps_on_square)
     elif mistake == "extra_rounding":
-        orig = om.ns_iteration
-        monkeypatch.setattr(om, "ns_iteration",
-                            lambda X, mode="fp64": orig(X, mode) if mode == "fp64" else _double_round_poly(X, mode))
+        orig = om.ns_poly
+        monkeypatch.setattr(om, "ns_poly", lambda A, mode="fp64": orig(A, mode) if mode == "fp64"
+                            else _double_round_poly(A))
     elif mistake == "no_nesterov":
         orig_m = om.momentum_update
         monkeypatch.setattr(om, "momentum_update", lambda g, b, mu, nest, mode="fp64": orig_m(g, b, mu, False, mode))
