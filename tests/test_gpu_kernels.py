@@ -41,7 +41,17 @@ def test_normalise_x0(shape, dtype):
     out = muon.ns5(to_dev(G, dtype), ns_steps=0)
     torch.cuda.synchronize()
     want = oracle.newton_schulz5(as_seen(G, dtype), 0, "bf16")
-    assert_bf16_close(bf16_np(out), want, 0.0, "X0", slack=0.0, max_frac=2e-3)
+    check_x0(bf16_np(out), want)
+
+
+def check_x0(got, want):
+    """X0 = bf16(Xb / (||Xb|| + 1e-7)): the GPU forms the norm and the quotient
+    in fp32, the oracle in fp64.  Xb has at most 256 significands per binade,
+    so when one significand's quotient lies within fp32 error of a bf16
+    midpoint every entry with that significand rounds the other way: entries
+    may differ by one bf16 spacing, a few percent of them at most."""
+    assert_bf16_close(got, want, 0.0, "X0", slack=0.0, max_frac=0.05)
+    assert rel(got, want) <= 2e-3
 
 
 @pytest.mark.parametrize("shape", SHAPES)
@@ -63,7 +73,7 @@ def test_one_step_each_kernel(shape):
     X1 = ws_view(ws, lay["x_offset"][1], m, n, ldx)
     # X0 is the oracle's normalised input (orientation: tall inputs transposed)
     Gv, tall = oracle.orient(G.astype(np.float64))
-    assert_bf16_close(X0, oracle.normalise(Gv, "bf16"), 0.0, "X0", slack=0.0, max_frac=2e-3)
+    check_x0(X0, oracle.normalise(Gv, "bf16"))
     # Gram kernel: exactly symmetric, A = bf16(X0 X0^T)
     assert np.array_equal(A, A.T)
     absX = np.abs(X0)
