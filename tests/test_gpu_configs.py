@@ -191,7 +191,7 @@ def test_orthogonal_input_flat_spectrum_at_8192():
     n = 8192
     g = torch.Generator(device="cuda").manual_seed(7)
     Q, _ = torch.linalg.qr(torch.randn((n, n), generator=g, device="cuda", dtype=torch.float32))
-    O = muon.ns5(Q, 5).float()
+    O = muon.ns5(Q.contiguous(), 5).float()
     s = torch.linalg.svdvals(O).double().cpu().numpy()
     a, b, c = oracle.NS_COEFFS
     x = 1.0 / (np.sqrt(n) + 1e-7)
