@@ -57,7 +57,8 @@ typedef enum muon_status {
   MUON_ERR_CUDA = -5,               /* a CUDA runtime call or launch failed */
   MUON_ERR_DEVICE_TIMEOUT = -6,     /* a bounded on-device wait expired (results invalid) */
   MUON_ERR_UNSUPPORTED_DEVICE = -7, /* the current device is not compute capability 10.3 */
-  MUON_ERR_TOO_LARGE = -8           /* a dimension exceeds 2^31-1 elements per row/matrix */
+  MUON_ERR_TOO_LARGE = -8,          /* a dimension exceeds 2^31-1 elements per row/matrix */
+  MUON_ERR_SCRATCH_LIMIT = -9       /* ns5_noalloc: the call needs more than its static scratch */
 } muon_status_t;
 
 typedef enum muon_dtype { MUON_BF16 = 0, MUON_F32 = 1 } muon_dtype_t;
@@ -153,6 +154,34 @@ int muon_set_debug(const char* key, long long value);
  * (X = a X + B X).  ms and launches are host arrays of n_kinds entries.
  * Returns 0, or -1 on a bad argument or a failed event query. */
 int muon_kernel_times(double* ms, int* launches, int n_kinds);
+
+/* Size of the static device scratch array used by ns5_noalloc. */
+#define MUON_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/* ns5 without a workspace argument, for callers that cannot allocate device
+ * memory: code hosted by a framework whose allocator owns the whole GPU and
+ * forbids side allocations, or code on a latency-critical path where
+ * cudaMalloc/cudaFree may synchronise the device.  The pages describe no
+ * counterpart; this is a convenience of this library.
+ *   G, g_dtype, O, batch, rows, cols, ns_steps, stream: exactly as in ns5;
+ *   the caller still provides G and O.
+ * The scratch ns5 would take from a workspace comes instead from one
+ * file-scope device array of MUON_NOALLOC_SCRATCH_BYTES (64 MiB).  That array
+ * occupies device memory on every GPU where the library's device code is
+ * loaded until the process exits.  Its device address is looked up on the
+ * first call made on each device (make that first call before any stream
+ * capture on that device).  Calls whose workspace need
+ * (ns5_workspace_size(batch, rows, cols)) exceeds the array return
+ * MUON_ERR_SCRATCH_LIMIT without launching anything; for example one 2048 x
+ * 2048 matrix or up to seven 1024 x 1024 matrices fit.  Every call shares the
+ * array and finds the previous call's contents in it (the call clears what
+ * must start at zero); calls that may overlap on the GPU -- on different
+ * streams or different host threads -- race on it and must be serialised by
+ * the caller.  Allocates nothing: no cudaMalloc, cudaFree or allocating
+ * library routine.  muon_device_status() is not available for these calls
+ * (the status word is inside the private array). */
+muon_status_t ns5_noalloc(const void* G, int g_dtype, void* O, int batch, int64_t rows,
+                          int64_t cols, int ns_steps, void* stream);
 
 #ifdef __cplusplus
 }

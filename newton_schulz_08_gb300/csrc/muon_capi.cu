@@ -639,6 +639,7 @@ const char* muon_status_str(muon_status_t s) {
     case MUON_ERR_DEVICE_TIMEOUT: return "bounded device wait expired";
     case MUON_ERR_UNSUPPORTED_DEVICE: return "current device is not compute capability 10.3 (sm_103)";
     case MUON_ERR_TOO_LARGE: return "dimension too large";
+    case MUON_ERR_SCRATCH_LIMIT: return "ns5_noalloc: problem needs more than the 64 MiB static scratch";
   }
   return "unknown status";
 }

@@ -25,13 +25,17 @@ MUON_ERR_CUDA = -5
 MUON_ERR_DEVICE_TIMEOUT = -6
 MUON_ERR_UNSUPPORTED_DEVICE = -7
 MUON_ERR_TOO_LARGE = -8
+MUON_ERR_SCRATCH_LIMIT = -9
 MUON_BF16 = 0
 MUON_F32 = 1
 
 #: every symbol include/muon.h declares
 EXPORTS = ["muon_workspace_size", "muon_step", "ns5_workspace_size", "ns5", "ns5_bank",
            "ns5_bank_workspace_size", "muon_device_status", "muon_status_str",
-           "ns5_workspace_layout", "muon_set_debug", "muon_kernel_times"]
+           "ns5_workspace_layout", "muon_set_debug", "muon_kernel_times", "ns5_noalloc"]
+
+#: bytes of the static device scratch ns5_noalloc uses (MUON_NOALLOC_SCRATCH_BYTES)
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 #: kernel kinds reported by muon_kernel_times
 KERNEL_KINDS = ["momentum_cast", "normalise", "gram", "poly", "update"]
@@ -92,6 +96,8 @@ def lib():
     L.muon_set_debug.restype = c_int
     L.muon_kernel_times.argtypes = [P(ctypes.c_double), P(c_int), c_int]
     L.muon_kernel_times.restype = c_int
+    L.ns5_noalloc.argtypes = [c_vp, c_int, c_vp, c_int, c_i64, c_i64, c_int, c_vp]
+    L.ns5_noalloc.restype = c_int
     _lib = L
     return L
 
@@ -242,3 +248,23 @@ def muon_kernel_times():
     if lib().muon_kernel_times(ms, cnt, n) != 0:
         raise RuntimeError("muon_kernel_times failed")
     return {k: (ms[i], cnt[i]) for i, k in enumerate(KERNEL_KINDS)}
+
+
+def ns5_noalloc(G, ns_steps=5, out=None, stream=None):
+    """ns5 without a workspace: the library's own static device scratch is
+    used (for callers that may not allocate device memory; see include/muon.h).
+    Only `out` is allocated here when the caller does not pass one."""
+    squeeze = G.dim() == 2
+    G3 = G.unsqueeze(0) if squeeze else G
+    if G3.dim() != 3 or not G3.is_contiguous():
+        raise ValueError("G must be a contiguous 2-D or 3-D tensor")
+    batch, rows, cols = G3.shape
+    if out is None:
+        out = torch.empty(G3.shape, dtype=torch.bfloat16, device=G.device)
+    if out.shape != G3.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bfloat16 tensor shaped like G")
+    st = lib().ns5_noalloc(ctypes.c_void_p(G3.data_ptr()), _dtype_code(G3),
+                           ctypes.c_void_p(out.data_ptr()), batch, rows, cols, int(ns_steps),
+                           _stream(stream))
+    _check(st, "ns5_noalloc")
+    return out[0] if squeeze else out
