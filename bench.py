@@ -5,7 +5,7 @@ q, k, v, o (768x768), c_fc (3072x768), c_proj (768x3072): 72 matrices, 84.93 M
 fp32 parameters, bf16 gradients, fp32 momentum buffers -- with fresh seeded
 gradients every step (three gradient sets, used in turn).  One step = one full
 Muon step over the bank: momentum, normalisation, 5 quintic Newton-Schulz
-steps, parameter update (17 kernel launches through the C ABI).
+steps, parameter update (18 kernel launches through the C ABI).
 
   value      matrices per second, device-timed with CUDA events on the
              launching stream, inputs resident in HBM (the bank's 0.85 GB of
@@ -78,7 +78,8 @@ def hbm_bytes(shapes, gbytes):
     """Algorithmic bytes of the elementwise passes for one step over the bank."""
     e = float(sum(r * c for r, c in shapes))
     return {"momentum_cast": e * (gbytes + 4 + 4 + 2),  # g, buf r/w, Xraw
-            "normalise": e * 4}                          # Xraw r, X0 w
+            "normalise": e * 4,                          # Xraw r, X0 w
+            "apply": e * (2 + 4 + 4)}                    # X r, p r/w
 
 
 def load_peaks():
@@ -405,7 +406,7 @@ def main():
                    "parallelism": f"replicas x{world}"},
         "ns5_tflops": total_flops / (ms * 1e-3) / 1e12,
         "ns5_tflops_note": "algorithmic NS FLOPs of the whole step / step time",
-        "update_gbs": (gbytes["momentum_cast"] + 8.0 * sum(r * c for r, c in shapes)) / (ms * 1e-3) / 1e9,
+        "update_gbs": (gbytes["momentum_cast"] + gbytes["apply"]) / (ms * 1e-3) / 1e9,
         "roofline": {"kernel": dom, "bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"],
                      "unit": d["unit"], "frac": d["frac"], "traffic": traffic,
                      "peak_source": f"{peak_src} ({'bf16_tflops burst' if d['unit'] == 'TFLOP/s' else 'hbm_gbs'})"},

@@ -138,8 +138,6 @@ muon_status_t ns5_workspace_layout(int batch, int64_t rows, int64_t cols, muon_w
  *   "inject_stall"        1: the Newton-Schulz kernels' MMA warp issues
  *                         nothing, so their waits expire (tests the bounded
  *                         wait path; combine with a small budget);
- *   "store_final_x"       1: the last B*X launch also stores the final X in
- *                         the workspace (as ns5_workspace_layout describes);
  *   "record_kernel_events" 1: every kernel launch is bracketed by a pair of
  *                         CUDA events recorded on the caller's stream (read
  *                         with muon_kernel_times; not for use under stream
@@ -151,7 +149,7 @@ int muon_set_debug(const char* key, long long value);
  * "record_kernel_events") and returns, per kernel kind, the summed
  * milliseconds and the launch count: kind 0 momentum_cast, 1 normalise,
  * 2 Gram (A = X X^T), 3 polynomial (B = b A + c A A), 4 update
- * (X = a X + B X).  ms and launches are host arrays of n_kinds entries.
+ * (X = a X + B X), 5 apply (p <- p - lr O, or O written).  ms and launches are host arrays of n_kinds entries.
  * Returns 0, or -1 on a bad argument or a failed event query. */
 int muon_kernel_times(double* ms, int* launches, int n_kinds);
 

@@ -15,8 +15,9 @@
 //   Xraw^2 per block (warp shuffles, then a fixed-order block reduction: the
 //   result does not depend on scheduling).
 // normalise: X0 = bf16(Xraw / (sqrt(sum of the matrix's partials) + 1e-7)),
-//   in place; the partials are summed in a fixed order by every block.  With
-//   zero Newton-Schulz steps it also applies the update (or writes O).
+//   in place; the partials are summed in a fixed order by every block.
+// apply: after the last step, p <- p - lr * O (or O written), O = X in the
+//   stored orientation.
 #include "plan.h"
 
 namespace muon {
@@ -154,26 +155,86 @@ __global__ void __launch_bounds__(kEwThreads) momentum_cast_kernel(const __grid_
   } else {
     // tall: X = u^T (C x R).  64 rows of u per block, 64 x 64 tiles through
     // shared memory so that both the reads of u and the writes of X are
-    // contiguous across a warp.
+    // contiguous across a warp.  Reads: a thread takes 4 consecutive
+    // columns of 4 rows (float4 buf, 8-byte bf16 g); writes: a thread stores
+    // 16 consecutive entries of one X row (two 16-byte stores).
     const int r0 = b * 64;
+    const int tid = threadIdx.x;
+    const bool vec_in = (C & 3) == 0;
     for (int c0 = 0; c0 < C; c0 += 64) {
-      for (int e = threadIdx.x; e < 64 * 64; e += kEwThreads) {
-        const int rr = e >> 6, cc = e & 63;
-        const int r = r0 + rr, c = c0 + cc;
-        float x = 0.0f;
-        if (r < R && c < C) {
+      const int cl = (tid & 15) * 4;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int rr = (tid >> 4) + 16 * k;
+        const int r = r0 + rr, c = c0 + cl;
+        float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (r < R && vec_in && c + 3 < C) {
           const long long i = static_cast<long long>(r) * C + c;
-          const float u = momentum_u(load_g(M.g, M.g_f32, i), M.buf, i, P.mu, P.nesterov);
-          x = bf16_round(u);
-          ss = fmaf(x, x, ss);
+          float g[4];
+          if (M.g_f32) {
+            const float4 v = *reinterpret_cast<const float4*>(static_cast<const float*>(M.g) + i);
+            g[0] = v.x; g[1] = v.y; g[2] = v.z; g[3] = v.w;
+          } else {
+            const uint2 v = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(M.g) + i);
+            g[0] = __uint_as_float(v.x << 16);
+            g[1] = __uint_as_float(v.x & 0xFFFF0000u);
+            g[2] = __uint_as_float(v.y << 16);
+            g[3] = __uint_as_float(v.y & 0xFFFF0000u);
+          }
+          float u[4];
+          if (M.buf) {
+            float4* bp = reinterpret_cast<float4*>(M.buf + i);
+            float4 bv = *bp;
+            bv.x = fmaf(P.mu, bv.x, g[0]);
+            bv.y = fmaf(P.mu, bv.y, g[1]);
+            bv.z = fmaf(P.mu, bv.z, g[2]);
+            bv.w = fmaf(P.mu, bv.w, g[3]);
+            *bp = bv;
+            u[0] = P.nesterov ? fmaf(P.mu, bv.x, g[0]) : bv.x;
+            u[1] = P.nesterov ? fmaf(P.mu, bv.y, g[1]) : bv.y;
+            u[2] = P.nesterov ? fmaf(P.mu, bv.z, g[2]) : bv.z;
+            u[3] = P.nesterov ? fmaf(P.mu, bv.w, g[3]) : bv.w;
+          } else {
+            u[0] = g[0]; u[1] = g[1]; u[2] = g[2]; u[3] = g[3];
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            x[j] = bf16_round(u[j]);
+            ss = fmaf(x[j], x[j], ss);
+          }
+        } else if (r < R) {
+          for (int j = 0; j < 4; ++j) {
+            if (c + j < C) {
+              const long long i = static_cast<long long>(r) * C + c + j;
+              const float u = momentum_u(load_g(M.g, M.g_f32, i), M.buf, i, P.mu, P.nesterov);
+              x[j] = bf16_round(u);
+              ss = fmaf(x[j], x[j], ss);
+            }
+          }
         }
-        tile[rr][cc] = x;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) tile[rr][cl + j] = x[j];
       }
       __syncthreads();
-      for (int e = threadIdx.x; e < 64 * 64; e += kEwThreads) {
-        const int cc = e >> 6, rr = e & 63;  // X row = c, X column = r
-        const int r = r0 + rr, c = c0 + cc;
-        if (r < R && c < C) M.x[static_cast<long long>(c) * M.ldx + r] = __float2bfloat16_rn(tile[rr][cc]);
+      {
+        const int cc = tid >> 2;          // X row c0 + cc
+        const int rb = (tid & 3) * 16;    // X columns r0 + rb .. + 15
+        const int c = c0 + cc;
+        if (c < C) {
+          __nv_bfloat16* xd = M.x + static_cast<long long>(c) * M.ldx + r0 + rb;
+          if (r0 + rb + 16 <= R) {
+            uint32_t w[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const __nv_bfloat162 h = __floats2bfloat162_rn(tile[rb + 2 * j][cc], tile[rb + 2 * j + 1][cc]);
+              w[j] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            reinterpret_cast<uint4*>(xd)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            reinterpret_cast<uint4*>(xd)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          } else {
+            for (int j = 0; j < 16 && r0 + rb + j < R; ++j) xd[j] = __float2bfloat16_rn(tile[rb + j][cc]);
+          }
+        }
       }
       __syncthreads();
     }
@@ -210,7 +271,7 @@ __global__ void __launch_bounds__(kEwThreads) normalise_kernel(const __grid_cons
   const int r0 = b * K.rows_per_block;
   const int r1 = min(K.m, r0 + K.rows_per_block);
   const int n = K.n;
-  if (P.final_mode == kFinalNone && (n & 7) == 0) {
+  if ((n & 7) == 0) {
     const int cv = n >> 3;
     const long long nvec = static_cast<long long>(r1 - r0) * cv;
     for (long long v = threadIdx.x; v < nvec; v += kEwThreads) {
@@ -234,17 +295,91 @@ __global__ void __launch_bounds__(kEwThreads) normalise_kernel(const __grid_cons
       const int r = r0 + static_cast<int>(e / n);
       const int cc = static_cast<int>(e % n);
       __nv_bfloat16* p = X + static_cast<long long>(r) * K.ldx + cc;
-      const __nv_bfloat16 x0 = __float2bfloat16_rn(__bfloat162float(*p) / d);
-      *p = x0;
-      if (P.final_mode != kFinalNone) {
-        // X is m x n; the matrix as stored is X (wide) or X^T (tall)
-        const long long o = mi.tall ? static_cast<long long>(cc) * K.m + r : static_cast<long long>(r) * n + cc;
+      *p = __float2bfloat16_rn(__bfloat162float(*p) / d);
+    }
+  }
+}
+
+// apply: O = X_final in the matrix's stored orientation; the Muon step does
+// p <- p - lr * O (fp32 FMA), Newton-Schulz alone writes O (bf16).  One
+// 64 x 64 tile of X per block.  Tall matrices (O = X^T) go through a shared
+// tile so that both the reads of X and the accesses to p / O are contiguous
+// across a warp.
+__global__ void __launch_bounds__(kEwThreads) apply_kernel(const __grid_constant__ ApplyParams P) {
+  __shared__ float tile[64][65];
+  int c = 0;
+  while (c + 1 < P.n_classes && (int)blockIdx.x >= P.cls[c + 1].tile_begin) ++c;
+  const ApplyClass& K = P.cls[c];
+  const int local = blockIdx.x - K.tile_begin;
+  const int per_mat = K.tiles_m * K.tiles_n;
+  const int idx = local / per_mat;
+  const int t = local - idx * per_mat;
+  const int r0 = (t / K.tiles_n) * 64;  // X rows
+  const int c0 = (t % K.tiles_n) * 64;  // X columns
+  const MatInfo mi = P.table[K.mat_begin + idx];
+  const __nv_bfloat16* X = K.x + static_cast<long long>(idx) * K.m * K.ldx;
+  const int m = K.m, n = K.n;
+  const int tid = threadIdx.x;
+  if (!mi.tall) {
+    // stored as X: element (r, c) at r * n + c; a thread handles 8 columns
+    // of two rows
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int r = r0 + (tid >> 3) + 32 * k;
+      const int cc = c0 + (tid & 7) * 8;
+      if (r >= m || cc >= n) continue;
+      const __nv_bfloat16* xs = X + static_cast<long long>(r) * K.ldx + cc;
+      const long long o = static_cast<long long>(r) * n + cc;
+      if ((n & 7) == 0) {
+        const uint4 w = *reinterpret_cast<const uint4*>(xs);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
         if (P.final_mode == kFinalParam) {
-          float* pp = static_cast<float*>(mi.out) + o;
-          *pp = fmaf(-P.lr, __bfloat162float(x0), *pp);
+          float4* pp = reinterpret_cast<float4*>(static_cast<float*>(mi.out) + o);
+          float4 a = pp[0], b = pp[1];
+          a.x = fmaf(-P.lr, __uint_as_float(ws[0] << 16), a.x);
+          a.y = fmaf(-P.lr, __uint_as_float(ws[0] & 0xFFFF0000u), a.y);
+          a.z = fmaf(-P.lr, __uint_as_float(ws[1] << 16), a.z);
+          a.w = fmaf(-P.lr, __uint_as_float(ws[1] & 0xFFFF0000u), a.w);
+          b.x = fmaf(-P.lr, __uint_as_float(ws[2] << 16), b.x);
+          b.y = fmaf(-P.lr, __uint_as_float(ws[2] & 0xFFFF0000u), b.y);
+          b.z = fmaf(-P.lr, __uint_as_float(ws[3] << 16), b.z);
+          b.w = fmaf(-P.lr, __uint_as_float(ws[3] & 0xFFFF0000u), b.w);
+          pp[0] = a;
+          pp[1] = b;
         } else {
-          static_cast<__nv_bfloat16*>(mi.out)[o] = x0;
+          *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(mi.out) + o) = w;
         }
+      } else {
+        for (int j = 0; j < 8 && cc + j < n; ++j) {
+          const __nv_bfloat16 x = xs[j];
+          if (P.final_mode == kFinalParam) {
+            float* pp = static_cast<float*>(mi.out) + o + j;
+            *pp = fmaf(-P.lr, __bfloat162float(x), *pp);
+          } else {
+            static_cast<__nv_bfloat16*>(mi.out)[o + j] = x;
+          }
+        }
+      }
+    }
+  } else {
+    // stored as X^T (n x m): element (c, r) at c * m + r
+    for (int e = tid; e < 64 * 64; e += kEwThreads) {
+      const int rr = e >> 6, cc = e & 63;
+      const int r = r0 + rr, col = c0 + cc;
+      tile[rr][cc] = (r < m && col < n) ? __bfloat162float(X[static_cast<long long>(r) * K.ldx + col]) : 0.0f;
+    }
+    __syncthreads();
+    for (int e = tid; e < 64 * 64; e += kEwThreads) {
+      const int cc = e >> 6, rr = e & 63;
+      const int r = r0 + rr, col = c0 + cc;
+      if (r >= m || col >= n) continue;
+      const long long o = static_cast<long long>(col) * m + r;
+      const float x = tile[rr][cc];
+      if (P.final_mode == kFinalParam) {
+        float* pp = static_cast<float*>(mi.out) + o;
+        *pp = fmaf(-P.lr, x, *pp);
+      } else {
+        static_cast<__nv_bfloat16*>(mi.out)[o] = __float2bfloat16_rn(x);
       }
     }
   }
@@ -255,6 +390,13 @@ cudaError_t launch_momentum_cast(const K1Params& P, int blocks, cudaStream_t str
   void* args[] = {const_cast<K1Params*>(&P)};
   return cudaLaunchKernel(reinterpret_cast<const void*>(&momentum_cast_kernel), dim3(blocks),
                           dim3(kEwThreads), args, 0, stream);
+}
+
+cudaError_t launch_apply(const ApplyParams& P, int blocks, cudaStream_t stream) {
+  if (blocks <= 0) return cudaSuccess;
+  void* args[] = {const_cast<ApplyParams*>(&P)};
+  return cudaLaunchKernel(reinterpret_cast<const void*>(&apply_kernel), dim3(blocks), dim3(kEwThreads), args,
+                          0, stream);
 }
 
 cudaError_t launch_normalise(const NormParams& P, int blocks, cudaStream_t stream) {

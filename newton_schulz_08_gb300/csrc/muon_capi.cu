@@ -8,8 +8,9 @@
 //                      transpose of tall matrices, partial norms
 //   normalise          1 launch: X0 = bf16(Xraw / (||Xraw||_F + 1e-7))
 //   ns_steps x { Gram, Poly, Update }   1 persistent launch each for the
-//                      whole bank (per group of <= 8 shape classes); the last
-//                      Update applies p <- p - lr O (or writes O).
+//                      whole bank (per group of <= 8 shape classes)
+//   apply              1 launch: p <- p - lr O (or O written), O = final X
+//                      transposed back for tall matrices
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -29,6 +30,7 @@ namespace muon {
 cudaError_t launch_ns_gemm(int mode, const GemmParams& P, int num_sms, cudaStream_t stream);
 cudaError_t launch_momentum_cast(const K1Params& P, int blocks, cudaStream_t stream);
 cudaError_t launch_normalise(const NormParams& P, int blocks, cudaStream_t stream);
+cudaError_t launch_apply(const ApplyParams& P, int blocks, cudaStream_t stream);
 
 namespace {
 
@@ -42,11 +44,10 @@ constexpr int kElemsPerBlock = 16384;  // elementwise passes: ~16K elements per 
 
 std::atomic<long long> g_wait_budget{4000000000LL};
 std::atomic<int> g_inject_stall{0};
-std::atomic<int> g_store_final_x{0};
 std::atomic<int> g_record_events{0};
 
 // Optional CUDA-event brackets around every launch (diagnostics).
-constexpr int kKinds = 5;  // momentum_cast, normalise, gram, poly, update
+// kinds: 0 momentum_cast, 1 normalise, 2 gram, 3 poly, 4 update, 5 apply
 struct EventPair {
   cudaEvent_t start, stop;
   int kind;
@@ -324,7 +325,7 @@ muon_status_t run(const std::vector<JobMat>& mats, const Plan& P, float lr, floa
     ev_end(ev, rec, stream);
   }
 
-  // normalise (and, for zero steps, the final output)
+  // normalise
   {
     for (size_t c0 = 0; c0 < P.cls.size(); c0 += kMaxClasses) {
       NormParams np;
@@ -346,8 +347,6 @@ muon_status_t run(const std::vector<JobMat>& mats, const Plan& P, float lr, floa
         blocks += cp.norm_blocks * cp.count;
       }
       np.n_classes = nc;
-      np.final_mode = ns_steps == 0 ? final_mode : kFinalNone;
-      np.lr = lr;
       np.partials = partials;
       np.table = table;
       np.status = status;
@@ -361,10 +360,8 @@ muon_status_t run(const std::vector<JobMat>& mats, const Plan& P, float lr, floa
   // Newton-Schulz steps
   const long long budget = g_wait_budget.load();
   const int stall = g_inject_stall.load();
-  const int store_final = g_store_final_x.load();
   for (int t = 0; t < ns_steps; ++t) {
     const int src = t & 1, dst = src ^ 1;
-    const bool last = t == ns_steps - 1;
     for (size_t c0 = 0; c0 < P.cls.size(); c0 += kMaxClasses) {
       const int nc = static_cast<int>(std::min<size_t>(kMaxClasses, P.cls.size() - c0));
       for (int mode = kGram; mode <= kUpdate; ++mode) {
@@ -428,10 +425,6 @@ muon_status_t run(const std::vector<JobMat>& mats, const Plan& P, float lr, floa
         gp.ca = kCoefA;
         gp.cb = kCoefB;
         gp.cc = kCoefC;
-        gp.final_mode = (mode == kUpdate && last) ? final_mode : kFinalNone;
-        gp.store_x = (mode == kUpdate) && (!last || store_final) ? 1 : 0;
-        gp.lr = lr;
-        gp.table = table;
         gp.status = status;
         gp.wait_budget = budget;
         gp.inject_stall = stall;
@@ -441,6 +434,37 @@ muon_status_t run(const std::vector<JobMat>& mats, const Plan& P, float lr, floa
         ev_end(ev, rec, stream);
       }
     }
+  }
+
+  // O = final X (transposed back); p <- p - lr O, or O written
+  const int fin = ns_steps & 1;
+  for (size_t c0 = 0; c0 < P.cls.size(); c0 += kMaxClasses) {
+    ApplyParams ap;
+    std::memset(&ap, 0, sizeof(ap));
+    const int nc = static_cast<int>(std::min<size_t>(kMaxClasses, P.cls.size() - c0));
+    int blocks = 0;
+    for (int j = 0; j < nc; ++j) {
+      const ClassPlan& cp = P.cls[c0 + j];
+      ApplyClass& k = ap.cls[j];
+      k.x = reinterpret_cast<const __nv_bfloat16*>(ws + cp.x_off[fin]);
+      k.count = cp.count;
+      k.m = cp.m;
+      k.n = cp.n;
+      k.ldx = cp.ldx;
+      k.mat_begin = cp.mat_begin;
+      k.tiles_m = static_cast<int>(ceil_div(cp.m, 64));
+      k.tiles_n = static_cast<int>(ceil_div(cp.n, 64));
+      k.tile_begin = blocks;
+      blocks += k.tiles_m * k.tiles_n * cp.count;
+    }
+    ap.n_classes = nc;
+    ap.final_mode = final_mode;
+    ap.lr = lr;
+    ap.table = table;
+    EventPair ev;
+    const bool rec = ev_begin(ev, 5, stream);
+    if (launch_apply(ap, blocks, stream) != cudaSuccess) return MUON_ERR_CUDA;
+    ev_end(ev, rec, stream);
   }
   return MUON_OK;
 }
@@ -676,10 +700,6 @@ int muon_set_debug(const char* key, long long value) {
   }
   if (!std::strcmp(key, "record_kernel_events")) {
     g_record_events.store(value ? 1 : 0);
-    return 0;
-  }
-  if (!std::strcmp(key, "store_final_x")) {
-    g_store_final_x.store(value ? 1 : 0);
     return 0;
   }
   return -1;

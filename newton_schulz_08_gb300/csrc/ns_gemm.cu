@@ -15,9 +15,8 @@
 //             reads A's tile and fuses b A + c (.).
 //   kUpdate : X' = a X + B X.     All tiles of the m x n result; B is the
 //             K-major operand, X the MN-major one.  The epilogue reads X's
-//             tile and fuses a X + (.).  On the last step it applies the
-//             parameter update p <- p - lr O (or writes O), transposing back
-//             matrices that were tall.
+//             tile and fuses a X + (.).  (The parameter update after the
+//             last step is a separate coalesced pass, apply_kernel.)
 //
 // Kernel structure (one CTA per SM, persistent over a static tile list that
 // spans all shape classes of the bank):
@@ -26,8 +25,10 @@
 //   warp 1     TMEM owner and MMA issuer: tcgen05.mma 128 x 256 x 16, fp32
 //              accumulators in TMEM, two accumulator buffers (2 x 256 columns)
 //              so the epilogue of one tile overlaps the main loop of the next.
-//   warps 2-5  epilogue: tcgen05.ld of 32 columns at a time, fused arithmetic,
-//              bfloat16 rounding, global stores.
+//   warps 2-9  epilogue: two warps per TMEM lane quarter, each owning half of
+//              the tile's 256 columns; the epilogue input row (A or X) is
+//              loaded before the accumulator is ready, then tcgen05.ld of 32
+//              columns at a time, fused arithmetic, bf16 rounding, stores.
 // Every barrier wait is bounded; on expiry the CTA raises the timeout bit of
 // the device status word, drains its own in-flight copies and MMAs, frees
 // TMEM and returns.
@@ -77,32 +78,9 @@ __device__ __forceinline__ void raise_timeout(const GemmParams& P, volatile int*
   atomicOr(P.status, kStatusTimeout);
 }
 
-__device__ __forceinline__ void unpack_bf16x2(uint32_t u, float& lo, float& hi) {
-  lo = __uint_as_float(u << 16);
-  hi = __uint_as_float(u & 0xFFFF0000u);
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-// Load 32 consecutive bf16 (row-major, starting at `src`) as floats.
-__device__ __forceinline__ void load_row32(const __nv_bfloat16* src, int valid, float (&v)[32]) {
-  if (valid >= 32) {
-    const uint4* s = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 w = s[q];
-      unpack_bf16x2(w.x, v[8 * q + 0], v[8 * q + 1]);
-      unpack_bf16x2(w.y, v[8 * q + 2], v[8 * q + 3]);
-      unpack_bf16x2(w.z, v[8 * q + 4], v[8 * q + 5]);
-      unpack_bf16x2(w.w, v[8 * q + 6], v[8 * q + 7]);
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = j < valid ? __bfloat162float(src[j]) : 0.0f;
-  }
 }
 
 // Store 32 packed bf16 (16 words) to `dst`, first `valid` elements only.
@@ -124,120 +102,79 @@ __device__ __forceinline__ uint16_t word_half(const uint32_t (&w)[16], int j) {
 }
 
 // ------------------------------------------------------------------ epilogues
+// 32 consecutive bf16 of one row as 16 packed words (zeros past `valid`).
+__device__ __forceinline__ void load_words32(const __nv_bfloat16* src, int valid, uint32_t (&w)[16]) {
+  if (valid >= 32) {
+    const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 v = s[q];
+      w[4 * q] = v.x;
+      w[4 * q + 1] = v.y;
+      w[4 * q + 2] = v.z;
+      w[4 * q + 3] = v.w;
+    }
+  } else {
+    const uint16_t* s = reinterpret_cast<const uint16_t*>(src);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t lo = 2 * j < valid ? s[2 * j] : 0u;
+      const uint32_t hi = 2 * j + 1 < valid ? s[2 * j + 1] : 0u;
+      w[j] = lo | (hi << 16);
+    }
+  }
+}
+
+__device__ __forceinline__ float word_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float word_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// One 32-column chunk of one tile row: `acc` from TMEM, `aux` the row's
+// epilogue input (A for the polynomial, X for the update; unused for Gram).
 template <int MODE>
 __device__ __forceinline__ void epilogue_chunk(const GemmParams& P, const GemmClass& C,
                                                const Tile& tl, int rg, int c0,
-                                               const uint32_t (&acc)[32]) {
-  if (MODE == kGram || MODE == kPoly) {
-    const int m = C.m;
-    if (rg >= m) return;
-    float v[32];
+                                               const uint32_t (&acc)[32], const uint32_t (&aux)[16]) {
+  uint32_t w[16];
+  if (MODE == kGram) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(acc[j]);
-    if (MODE == kPoly) {
-      float a[32];
-      const __nv_bfloat16* src = C.aux + tl.idx * C.aux_mat_stride + static_cast<long long>(rg) * C.ld_aux + c0;
-      load_row32(src, m - c0, a);
+    for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(__uint_as_float(acc[2 * j]), __uint_as_float(acc[2 * j + 1]));
+  } else if (MODE == kPoly) {
+    // B = b A + c (A A)
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = fmaf(P.cb, a[j], P.cc * v[j]);
-    }
-    uint32_t w[16];
+    for (int j = 0; j < 16; ++j)
+      w[j] = pack_bf16x2(fmaf(P.cb, word_lo(aux[j]), P.cc * __uint_as_float(acc[2 * j])),
+                         fmaf(P.cb, word_hi(aux[j]), P.cc * __uint_as_float(acc[2 * j + 1])));
+  } else {
+    // X' = a X + B X
 #pragma unroll
-    for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
-    __nv_bfloat16* out = C.out + tl.idx * C.out_mat_stride;
-    // direct: entries with rg <= c
-    __nv_bfloat16* drow = out + static_cast<long long>(rg) * C.ld_out + c0;
-    if (c0 >= rg) {
-      store_row32(drow, m - c0, w);
-    } else {
-      uint16_t* d = reinterpret_cast<uint16_t*>(drow);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int c = c0 + j;
-        if (c >= rg && c < m) d[j] = word_half(w, j);
-      }
-    }
-    // mirror: entries with rg < c go to (c, rg); a warp writes 32 adjacent rg
-    uint16_t* mcol = reinterpret_cast<uint16_t*>(out) + rg;
+    for (int j = 0; j < 16; ++j)
+      w[j] = pack_bf16x2(fmaf(P.ca, word_lo(aux[j]), __uint_as_float(acc[2 * j])),
+                         fmaf(P.ca, word_hi(aux[j]), __uint_as_float(acc[2 * j + 1])));
+  }
+  __nv_bfloat16* out = C.out + tl.idx * C.out_mat_stride;
+  if (MODE == kUpdate) {
+    store_row32(out + static_cast<long long>(rg) * C.ld_out + c0, C.n - c0, w);
+    return;
+  }
+  const int m = C.m;
+  // direct: entries with rg <= c
+  __nv_bfloat16* drow = out + static_cast<long long>(rg) * C.ld_out + c0;
+  if (c0 >= rg) {
+    store_row32(drow, m - c0, w);
+  } else {
+    uint16_t* d = reinterpret_cast<uint16_t*>(drow);
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       const int c = c0 + j;
-      if (c > rg && c < m) mcol[static_cast<long long>(c) * C.ld_out] = word_half(w, j);
+      if (c >= rg && c < m) d[j] = word_half(w, j);
     }
-  } else {
-    const int m = C.m, n = C.n;
-    if (rg >= m) return;
-    const int valid = n - c0;
-    float x[32];
-    const __nv_bfloat16* xs = C.aux + tl.idx * C.aux_mat_stride + static_cast<long long>(rg) * C.ld_aux + c0;
-    load_row32(xs, valid, x);
-    uint32_t w[16];
+  }
+  // mirror: entries with rg < c go to (c, rg); a warp writes 32 adjacent rg
+  uint16_t* mcol = reinterpret_cast<uint16_t*>(out) + rg;
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
-      w[j] = pack_bf16x2(fmaf(P.ca, x[2 * j], __uint_as_float(acc[2 * j])),
-                         fmaf(P.ca, x[2 * j + 1], __uint_as_float(acc[2 * j + 1])));
-    if (P.store_x) {
-      __nv_bfloat16* xd = C.out + tl.idx * C.out_mat_stride + static_cast<long long>(rg) * C.ld_out + c0;
-      store_row32(xd, valid, w);
-    }
-    if (P.final_mode != kFinalNone) {
-      const MatInfo mi = P.table[C.mat_begin + tl.idx];
-      if (P.final_mode == kFinalParam) {
-        float* p = static_cast<float*>(mi.out);
-        if (!mi.tall) {
-          float* prow = p + static_cast<long long>(rg) * n + c0;
-          if (valid >= 32 && (n & 3) == 0) {
-            float4* p4 = reinterpret_cast<float4*>(prow);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              float4 t = p4[q];
-              float o0, o1, o2, o3;
-              unpack_bf16x2(w[2 * q], o0, o1);
-              unpack_bf16x2(w[2 * q + 1], o2, o3);
-              t.x = fmaf(-P.lr, o0, t.x);
-              t.y = fmaf(-P.lr, o1, t.y);
-              t.z = fmaf(-P.lr, o2, t.z);
-              t.w = fmaf(-P.lr, o3, t.w);
-              p4[q] = t;
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (j < valid) {
-                float o = __uint_as_float(static_cast<uint32_t>(word_half(w, j)) << 16);
-                prow[j] = fmaf(-P.lr, o, prow[j]);
-              }
-            }
-          }
-        } else {
-          // tall: O = X^T, p is n x m; a warp covers 32 adjacent rg
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (j < valid) {
-              float* pe = p + static_cast<long long>(c0 + j) * m + rg;
-              float o = __uint_as_float(static_cast<uint32_t>(word_half(w, j)) << 16);
-              *pe = fmaf(-P.lr, o, *pe);
-            }
-          }
-        }
-      } else {
-        uint16_t* o = static_cast<uint16_t*>(mi.out);
-        if (!mi.tall) {
-          uint16_t* orow = o + static_cast<long long>(rg) * n + c0;
-          if ((n & 7) == 0) {
-            store_row32(reinterpret_cast<__nv_bfloat16*>(orow), valid, w);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j < valid) orow[j] = word_half(w, j);
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < valid) o[static_cast<long long>(c0 + j) * m + rg] = word_half(w, j);
-        }
-      }
-    }
+  for (int j = 0; j < 32; ++j) {
+    const int c = c0 + j;
+    if (c > rg && c < m) mcol[static_cast<long long>(c) * C.ld_out] = word_half(w, j);
   }
 }
 
@@ -267,7 +204,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(ptx::smem_addr(&tfull[a]), 1);
-      ptx::mbar_init(ptx::smem_addr(&tempty[a]), 128);
+      ptx::mbar_init(ptx::smem_addr(&tempty[a]), 32 * kEpiWarps);
     }
     ptx::mbar_init(ptx::smem_addr(drain), 1);
     *abort = 0;
@@ -385,7 +322,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     }
   } else {
     // -------------------------------------------------------------- epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // Warp w (2..9) reads TMEM lane quarter w % 4 (rows 32q..32q+31 of the
+    // tile) and the column half (w - 2) / 4 (chunks 4h .. 4h+3 of 32 columns).
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row_in_tile = q * 32 + lane;
     int it = 0;
     for (int t = blockIdx.x; t < P.total_tiles; t += gridDim.x, ++it) {
@@ -393,25 +333,42 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       const GemmClass& C = P.cls[tl.cls];
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
+      const int rg = tl.I * kBM + row_in_tile;
+      const int warp_row0 = tl.I * kBM + q * 32;
+      const int ncols = MODE == kUpdate ? C.n : C.m;
+      const int cbase = tl.J * kBN + half * (kBN / 2);
+      // this thread's epilogue input for its 128 columns, loaded before the
+      // accumulator is ready so that the loads overlap the main loop
+      uint32_t aux[4][16];
+      if (MODE != kGram) {
+        const __nv_bfloat16* arow = C.aux + tl.idx * C.aux_mat_stride + static_cast<long long>(rg) * C.ld_aux;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          const int c0 = cbase + ch * 32;
+          if (rg < C.m && c0 < ncols) {
+            load_words32(arow + c0, ncols - c0, aux[ch]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) aux[ch][j] = 0u;
+          }
+        }
+      }
       if (!ptx::mbar_wait(ptx::smem_addr(&tfull[acc]), acc_phase, budget, abort)) {
         raise_timeout(P, abort);
         break;
       }
       ptx::tc_fence_after();
-      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
-      const int rg = tl.I * kBM + row_in_tile;
-      const int warp_row0 = tl.I * kBM + q * 32;
-      const int ncols = MODE == kUpdate ? C.n : C.m;
-#pragma unroll 1
-      for (int ch = 0; ch < kBN / 32; ++ch) {
-        const int c0 = tl.J * kBN + ch * 32;
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN + half * (kBN / 2);
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        const int c0 = cbase + ch * 32;
         if (c0 >= ncols) break;  // warp-uniform
         if (MODE != kUpdate && c0 + 31 < warp_row0) continue;  // strictly below the diagonal
         uint32_t r[32];
         __syncwarp();
         ptx::tmem_ld32(tb + ch * 32, r);
         ptx::tmem_ld_wait();
-        epilogue_chunk<MODE>(P, C, tl, rg, c0, r);
+        if (rg < C.m) epilogue_chunk<MODE>(P, C, tl, rg, c0, r, aux[ch]);
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(ptx::smem_addr(&tempty[acc]));

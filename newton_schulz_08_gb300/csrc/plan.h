@@ -74,8 +74,6 @@ struct NormClass {
 struct NormParams {
   NormClass cls[kMaxClasses];
   int n_classes;
-  int final_mode;     // ns_steps == 0: write O / update p here
-  float lr;
   const float* partials;
   const MatInfo* table;
   int* status;
@@ -103,14 +101,29 @@ struct GemmParams {
   int n_classes;
   int total_tiles;
   float ca, cb, cc;             // Newton-Schulz coefficients
-  int final_mode;
-  int store_x;                  // update: also store X_{t+1}
-  float lr;
-  const MatInfo* table;
   int* status;
   long long wait_budget;        // clock64 cycles per barrier wait
   int inject_stall;             // test hook: MMA warp issues nothing
   int pad;
+};
+
+// ---------------------------------------------------------------- apply
+// Final pass: O = X (transposed back for tall matrices); the Muon step
+// applies p <- p - lr * O, Newton-Schulz alone writes O.  64 x 64 tiles of X.
+struct ApplyClass {
+  const __nv_bfloat16* x;  // final X buffer of the class, count x m x ldx
+  int count, m, n, ldx;
+  int mat_begin;
+  int tiles_m, tiles_n;    // 64 x 64 tiles per matrix
+  int tile_begin;
+};
+
+struct ApplyParams {
+  ApplyClass cls[kMaxClasses];
+  int n_classes;
+  int final_mode;          // kFinalParam or kFinalOut
+  float lr;
+  const MatInfo* table;
 };
 
 // tile sizes of the tcgen05 kernels
@@ -122,6 +135,7 @@ constexpr int kStageA = kBM * kBK * 2;        // 16 KB
 constexpr int kStageB = kBN * kBK * 2;        // 32 KB
 constexpr int kStageBytes = kStageA + kStageB;
 constexpr int kGemmSmem = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
-constexpr int kGemmThreads = 192;
+constexpr int kEpiWarps = 8;     // two warps per TMEM lane quarter, one per column half
+constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 
 }  // namespace muon

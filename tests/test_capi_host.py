@@ -184,4 +184,4 @@ def test_set_debug_keys(L):
     assert L.muon_set_debug(b"no_such_key", 1) == -1
     assert L.muon_set_debug(b"wait_budget_cycles", 4000000000) == 0
     assert L.muon_set_debug(b"inject_stall", 0) == 0
-    assert L.muon_set_debug(b"store_final_x", 0) == 0
+    assert L.muon_set_debug(b"record_kernel_events", 0) == 0

@@ -63,13 +63,9 @@ def test_single_128x512():
     P, Bd, Gd = to_dev(p), to_dev(b), to_dev(g)
     lay = muon.ns5_workspace_layout(1, R, C)
     ws = muon.new_workspace(muon.muon_workspace_size([(R, C)]))
-    muon.muon_set_debug("store_final_x", 1)
-    try:
-        muon.muon_step([P], [Gd], [Bd], lr=cfg["lr"], momentum=cfg["momentum"], nesterov=True,
-                       ns_steps=cfg["ns_steps"], workspace=ws)
-        check_status(ws)
-    finally:
-        muon.muon_set_debug("store_final_x", 0)
+    muon.muon_step([P], [Gd], [Bd], lr=cfg["lr"], momentum=cfg["momentum"], nesterov=True,
+                   ns_steps=cfg["ns_steps"], workspace=ws)
+    check_status(ws)
     new_p, new_buf, O = oracle.muon_step(p, g, b, LR, MU, True, 5, "bf16")
     # (i) momentum buffer
     assert rel(Bd.cpu().numpy(), new_buf) <= TOL_BUF_REL

@@ -60,12 +60,8 @@ def test_one_step_each_kernel(shape):
     G = gauss(shape, 2)
     lay = muon.ns5_workspace_layout(1, R, C)
     ws = muon.new_workspace(muon.ns5_workspace_size(1, R, C))
-    muon.muon_set_debug("store_final_x", 1)
-    try:
-        out = muon.ns5(to_dev(G), ns_steps=1, workspace=ws)
-        check_status(ws)
-    finally:
-        muon.muon_set_debug("store_final_x", 0)
+    out = muon.ns5(to_dev(G), ns_steps=1, workspace=ws)
+    check_status(ws)
     m, n, ldx, lda = lay["m"], lay["n"], lay["ldx"], lay["lda"]
     X0 = ws_view(ws, lay["x_offset"][0], m, n, ldx)
     A = ws_view(ws, lay["a_offset"], m, m, lda)
@@ -166,12 +162,8 @@ def test_param_update_is_exact_given_gpu_O():
     P, Gd, Bd = to_dev(p), to_dev(g), to_dev(b)
     lay = muon.ns5_workspace_layout(1, R, C)
     ws = muon.new_workspace(muon.muon_workspace_size([(R, C)]))
-    muon.muon_set_debug("store_final_x", 1)
-    try:
-        muon.muon_step([P], [Gd], [Bd], lr=0.02, momentum=0.95, ns_steps=5, workspace=ws)
-        check_status(ws)
-    finally:
-        muon.muon_set_debug("store_final_x", 0)
+    muon.muon_step([P], [Gd], [Bd], lr=0.02, momentum=0.95, ns_steps=5, workspace=ws)
+    check_status(ws)
     X5 = ws_view(ws, lay["x_offset"][1], lay["m"], lay["n"], lay["ldx"])  # 5 steps end in buffer 1
     O = X5.T  # tall
     want = (p - np.float32(0.02) * O.astype(np.float32)).astype(np.float32)
