@@ -138,6 +138,16 @@ muon_status_t ns5_workspace_layout(int batch, int64_t rows, int64_t cols, muon_w
  *   "inject_stall"        1: the Newton-Schulz kernels' MMA warp issues
  *                         nothing, so their waits expire (tests the bounded
  *                         wait path; combine with a small budget);
+ *   "wait_profile_buffer" device address of a zeroed int64 array of
+ *                         3 x 256 x 8 entries, or 0 to switch off:
+ *                         each Newton-Schulz kernel CTA adds clock64 cycles
+ *                         spent waiting per role (producer for free stages,
+ *                         MMA issuer for operands / for a drained
+ *                         accumulator, epilogue for an accumulator), the
+ *                         epilogue's busy cycles, the whole kernel's cycles,
+ *                         its tile count and the MMA loop's cycles, in that
+ *                         order, at ((kind x 256) + CTA index) x 8 with kind
+ *                         0 Gram, 1 polynomial, 2 update;
  *   "record_kernel_events" 1: every kernel launch is bracketed by a pair of
  *                         CUDA events recorded on the caller's stream (read
  *                         with muon_kernel_times; not for use under stream

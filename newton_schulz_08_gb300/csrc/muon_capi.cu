@@ -45,6 +45,7 @@ constexpr int kElemsPerBlock = 16384;  // elementwise passes: ~16K elements per 
 std::atomic<long long> g_wait_budget{4000000000LL};
 std::atomic<int> g_inject_stall{0};
 std::atomic<int> g_record_events{0};
+std::atomic<long long> g_wait_profile{0};  // device address of the counters, 0: off
 
 // Optional CUDA-event brackets around every launch (diagnostics).
 // kinds: 0 momentum_cast, 1 normalise, 2 gram, 3 poly, 4 update, 5 apply
@@ -267,11 +268,10 @@ bool encode_map(CUtensorMap* map, void* base, int cols, int rows, int count, int
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// square kBM x kBN tiles on and above the diagonal
 int sym_tiles_per_mat(int m) {
-  const int tm = static_cast<int>(ceil_div(m, kBM)), tn = static_cast<int>(ceil_div(m, kBN));
-  int t = 0;
-  for (int J = 0; J < tn; ++J) t += std::min(2 * J + 2, tm);
-  return t;
+  const int tn = static_cast<int>(ceil_div(m, kBN));
+  return tn * (tn + 1) / 2;
 }
 
 // ------------------------------------------------------------------ the run
@@ -376,32 +376,28 @@ muon_status_t run(const std::vector<JobMat>& mats, const Plan& P, float lr, floa
           void* A = ws + cp.a_off;
           void* B = ws + cp.b_off;
           bool ok = true;
+          // operands: A rows (box 64 x 128 per CTA), B rows or X columns;
+          // epilogue: input tile, output tile (64 x 128), mirrored block (64 x 256)
           if (mode == kGram) {
-            ok = encode_map(&g.tmA, xs, cp.n, cp.m, cp.count, cp.ldx, kBK, kBM) &&
-                 encode_map(&g.tmB, xs, cp.n, cp.m, cp.count, cp.ldx, kBK, kBM);
-            g.out = static_cast<__nv_bfloat16*>(A);
-            g.ld_out = cp.lda;
-            g.out_mat_stride = static_cast<long long>(cp.m) * cp.lda;
+            ok = encode_map(&g.tmA, xs, cp.n, cp.m, cp.count, cp.ldx, kBK, kBM / 2) &&
+                 encode_map(&g.tmB, xs, cp.n, cp.m, cp.count, cp.ldx, kBK, kBN / 2) &&
+                 encode_map(&g.tmAux, A, cp.m, cp.m, cp.count, cp.lda, 64, kBM / 2) &&
+                 encode_map(&g.tmOut, A, cp.m, cp.m, cp.count, cp.lda, 64, kBM / 2) &&
+                 encode_map(&g.tmOutT, A, cp.m, cp.m, cp.count, cp.lda, 64, kBN);
             g.K = cp.n;
           } else if (mode == kPoly) {
-            ok = encode_map(&g.tmA, A, cp.m, cp.m, cp.count, cp.lda, kBK, kBM) &&
-                 encode_map(&g.tmB, A, cp.m, cp.m, cp.count, cp.lda, kBK, kBM);
-            g.out = static_cast<__nv_bfloat16*>(B);
-            g.ld_out = cp.lda;
-            g.out_mat_stride = static_cast<long long>(cp.m) * cp.lda;
-            g.aux = static_cast<const __nv_bfloat16*>(A);
-            g.ld_aux = cp.lda;
-            g.aux_mat_stride = static_cast<long long>(cp.m) * cp.lda;
+            ok = encode_map(&g.tmA, A, cp.m, cp.m, cp.count, cp.lda, kBK, kBM / 2) &&
+                 encode_map(&g.tmB, A, cp.m, cp.m, cp.count, cp.lda, kBK, kBN / 2) &&
+                 encode_map(&g.tmAux, A, cp.m, cp.m, cp.count, cp.lda, 64, kBM / 2) &&
+                 encode_map(&g.tmOut, B, cp.m, cp.m, cp.count, cp.lda, 64, kBM / 2) &&
+                 encode_map(&g.tmOutT, B, cp.m, cp.m, cp.count, cp.lda, 64, kBN);
             g.K = cp.m;
           } else {
-            ok = encode_map(&g.tmA, B, cp.m, cp.m, cp.count, cp.lda, kBK, kBM) &&
-                 encode_map(&g.tmB, xs, cp.n, cp.m, cp.count, cp.ldx, 64, kBK);
-            g.out = static_cast<__nv_bfloat16*>(xd);
-            g.ld_out = cp.ldx;
-            g.out_mat_stride = static_cast<long long>(cp.m) * cp.ldx;
-            g.aux = static_cast<const __nv_bfloat16*>(xs);
-            g.ld_aux = cp.ldx;
-            g.aux_mat_stride = static_cast<long long>(cp.m) * cp.ldx;
+            ok = encode_map(&g.tmA, B, cp.m, cp.m, cp.count, cp.lda, kBK, kBM / 2) &&
+                 encode_map(&g.tmB, xs, cp.n, cp.m, cp.count, cp.ldx, 64, kBK) &&
+                 encode_map(&g.tmAux, xs, cp.n, cp.m, cp.count, cp.ldx, 64, kBM / 2) &&
+                 encode_map(&g.tmOut, xd, cp.n, cp.m, cp.count, cp.ldx, 64, kBM / 2) &&
+                 encode_map(&g.tmOutT, xd, cp.n, cp.m, cp.count, cp.ldx, 64, kBM / 2);
             g.K = cp.m;
           }
           if (!ok) return MUON_ERR_CUDA;
@@ -428,6 +424,7 @@ muon_status_t run(const std::vector<JobMat>& mats, const Plan& P, float lr, floa
         gp.status = status;
         gp.wait_budget = budget;
         gp.inject_stall = stall;
+        gp.wait_profile = reinterpret_cast<long long*>(g_wait_profile.load());
         EventPair ev;
         const bool rec = ev_begin(ev, 2 + mode, stream);
         if (launch_ns_gemm(mode, gp, sms, stream) != cudaSuccess) return MUON_ERR_CUDA;
@@ -696,6 +693,10 @@ int muon_set_debug(const char* key, long long value) {
   }
   if (!std::strcmp(key, "inject_stall")) {
     g_inject_stall.store(value ? 1 : 0);
+    return 0;
+  }
+  if (!std::strcmp(key, "wait_profile_buffer")) {
+    g_wait_profile.store(value);
     return 0;
   }
   if (!std::strcmp(key, "record_kernel_events")) {

@@ -18,20 +18,27 @@
 //             tile and fuses a X + (.).  (The parameter update after the
 //             last step is a separate coalesced pass, apply_kernel.)
 //
-// Kernel structure (one CTA per SM, persistent over a static tile list that
-// spans all shape classes of the bank):
-//   warp 0     TMA producer: 4-stage ring of (128 x 64) A and (256 x 64) B
-//              tiles, 128-byte swizzle, one mbarrier pair per stage.
-//   warp 1     TMEM owner and MMA issuer: tcgen05.mma 128 x 256 x 16, fp32
-//              accumulators in TMEM, two accumulator buffers (2 x 256 columns)
-//              so the epilogue of one tile overlaps the main loop of the next.
-//   warps 2-9  epilogue: two warps per TMEM lane quarter, each owning half of
-//              the tile's 256 columns; the epilogue input row (A or X) is
-//              loaded before the accumulator is ready, then tcgen05.ld of 32
-//              columns at a time, fused arithmetic, bf16 rounding, stores.
-// Every barrier wait is bounded; on expiry the CTA raises the timeout bit of
-// the device status word, drains its own in-flight copies and MMAs, frees
-// TMEM and returns.
+// Kernel structure: clusters of two CTAs on neighbouring SMs; each pair
+// computes 256 x 256 output tiles with tcgen05.mma.cta_group::2 (M = 256 over
+// the pair), persistent over a static tile list that spans all shape classes
+// of the bank.  Per CTA:
+//   warp 0     TMA producer: 6-stage ring of this CTA's halves, (128 x 64) A
+//              rows and (128 x 64) B columns, 128-byte swizzle; completion is
+//              counted on the leader CTA's full barrier.
+//   warp 1     TMEM allocation (both CTAs, 2 x 256 fp32 accumulator columns);
+//              in the leader CTA one thread issues the MMAs 256 x 256 x 16
+//              and commits to the stage / accumulator barriers of both CTAs.
+//   warps 2-9  epilogue of this CTA's 128 accumulator rows: two warps per
+//              TMEM lane quarter, each owning half of the 256 columns; the
+//              epilogue input row (A or X) is loaded before the accumulator
+//              is ready, then tcgen05.ld of 32 columns at a time, fused
+//              arithmetic, bf16 rounding, stores; finally an arrive on the
+//              leader's accumulator-empty barrier.
+// Each CTA moves 32 KB per 64-deep K block for 2 x 128 x 256 x 64 MACs of
+// the pair: a third less operand traffic per FLOP than single-CTA
+// 128 x 256 tiles.  Every barrier wait is bounded; on expiry the CTA raises
+// the timeout bit of the device status word, lets its copies and MMAs
+// drain, frees TMEM and returns.
 #include "plan.h"
 #include "ptx.cuh"
 
@@ -58,11 +65,12 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& P, int t) {
     r.I = q % C.tiles_m;
     r.J = q / C.tiles_m;
   } else {
-    // column block J holds row blocks 0 .. min(2J+1, tiles_m-1)
+    // square tiles on and above the diagonal: column block J holds row
+    // blocks 0 .. J
     int J = 0;
 #pragma unroll 1
     while (true) {
-      const int cnt = min(2 * J + 2, C.tiles_m);
+      const int cnt = J + 1;
       if (q < cnt) break;
       q -= cnt;
       ++J;
@@ -83,100 +91,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Store 32 packed bf16 (16 words) to `dst`, first `valid` elements only.
-__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, int valid, const uint32_t (&w)[16]) {
-  if (valid >= 32) {
-    uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) d[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-  } else {
-    uint16_t* d = reinterpret_cast<uint16_t*>(dst);
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (j < valid) d[j] = static_cast<uint16_t>((w[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
-  }
-}
-
-__device__ __forceinline__ uint16_t word_half(const uint32_t (&w)[16], int j) {
-  return static_cast<uint16_t>((w[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
-}
-
-// ------------------------------------------------------------------ epilogues
-// 32 consecutive bf16 of one row as 16 packed words (zeros past `valid`).
-__device__ __forceinline__ void load_words32(const __nv_bfloat16* src, int valid, uint32_t (&w)[16]) {
-  if (valid >= 32) {
-    const uint4* s = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 v = s[q];
-      w[4 * q] = v.x;
-      w[4 * q + 1] = v.y;
-      w[4 * q + 2] = v.z;
-      w[4 * q + 3] = v.w;
-    }
-  } else {
-    const uint16_t* s = reinterpret_cast<const uint16_t*>(src);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const uint32_t lo = 2 * j < valid ? s[2 * j] : 0u;
-      const uint32_t hi = 2 * j + 1 < valid ? s[2 * j + 1] : 0u;
-      w[j] = lo | (hi << 16);
-    }
-  }
-}
-
 __device__ __forceinline__ float word_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float word_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// One 32-column chunk of one tile row: `acc` from TMEM, `aux` the row's
-// epilogue input (A for the polynomial, X for the update; unused for Gram).
-template <int MODE>
-__device__ __forceinline__ void epilogue_chunk(const GemmParams& P, const GemmClass& C,
-                                               const Tile& tl, int rg, int c0,
-                                               const uint32_t (&acc)[32], const uint32_t (&aux)[16]) {
-  uint32_t w[16];
-  if (MODE == kGram) {
-#pragma unroll
-    for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(__uint_as_float(acc[2 * j]), __uint_as_float(acc[2 * j + 1]));
-  } else if (MODE == kPoly) {
-    // B = b A + c (A A)
-#pragma unroll
-    for (int j = 0; j < 16; ++j)
-      w[j] = pack_bf16x2(fmaf(P.cb, word_lo(aux[j]), P.cc * __uint_as_float(acc[2 * j])),
-                         fmaf(P.cb, word_hi(aux[j]), P.cc * __uint_as_float(acc[2 * j + 1])));
-  } else {
-    // X' = a X + B X
-#pragma unroll
-    for (int j = 0; j < 16; ++j)
-      w[j] = pack_bf16x2(fmaf(P.ca, word_lo(aux[j]), __uint_as_float(acc[2 * j])),
-                         fmaf(P.ca, word_hi(aux[j]), __uint_as_float(acc[2 * j + 1])));
-  }
-  __nv_bfloat16* out = C.out + tl.idx * C.out_mat_stride;
-  if (MODE == kUpdate) {
-    store_row32(out + static_cast<long long>(rg) * C.ld_out + c0, C.n - c0, w);
-    return;
-  }
-  const int m = C.m;
-  // direct: entries with rg <= c
-  __nv_bfloat16* drow = out + static_cast<long long>(rg) * C.ld_out + c0;
-  if (c0 >= rg) {
-    store_row32(drow, m - c0, w);
-  } else {
-    uint16_t* d = reinterpret_cast<uint16_t*>(drow);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int c = c0 + j;
-      if (c >= rg && c < m) d[j] = word_half(w, j);
-    }
-  }
-  // mirror: entries with rg < c go to (c, rg); a warp writes 32 adjacent rg
-  uint16_t* mcol = reinterpret_cast<uint16_t*>(out) + rg;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const int c = c0 + j;
-    if (c > rg && c < m) mcol[static_cast<long long>(c) * C.ld_out] = word_half(w, j);
-  }
-}
 
 }  // namespace
 
@@ -184,18 +100,26 @@ template <int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + kStages;
-  uint64_t* tfull = bars + 2 * kStages;
-  uint64_t* tempty = bars + 2 * kStages + 2;
+  uint8_t* stg = smem + kStages * kStageBytes;  // epilogue staging tile
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stg + kStageOut);
+  uint64_t* full = bars;                       // leader: both CTAs' tiles landed
+  uint64_t* empty = bars + kStages;            // stage free in this CTA
+  uint64_t* tfull = bars + 2 * kStages;        // accumulator ready (this CTA's lanes)
+  uint64_t* tempty = bars + 2 * kStages + 2;   // leader: both CTAs drained it
   uint64_t* drain = bars + 2 * kStages + 4;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+  uint64_t* aux_full = bars + 2 * kStages + 5; // epilogue input tile landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 6);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* never = reinterpret_cast<volatile int*>(tmem_slot + 2);  // stays 0
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const long long t_start = clock64();
+  long long* prof = P.wait_profile ? P.wait_profile + (MODE * 256 + static_cast<long long>(blockIdx.x)) * kWaitCounters
+                                   : nullptr;
+  const uint32_t rank = ptx::cluster_ctarank();  // 0: leader (issues the MMAs)
+  const int pair = static_cast<int>(ptx::cluster_id_x());
+  const int npairs = static_cast<int>(ptx::nclusters_x());
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -204,19 +128,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(ptx::smem_addr(&tfull[a]), 1);
-      ptx::mbar_init(ptx::smem_addr(&tempty[a]), 32 * kEpiWarps);
+      ptx::mbar_init(ptx::smem_addr(&tempty[a]), 2 * kEpiWarps);
     }
     ptx::mbar_init(ptx::smem_addr(drain), 1);
+    ptx::mbar_init(ptx::smem_addr(aux_full), 1);
     *abort = 0;
     *never = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), 512);
-    ptx::tmem_relinquish();
+    ptx::tmem_alloc_pair(ptx::smem_addr(tmem_slot), 512);
+    ptx::tmem_relinquish_pair();
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  ptx::cluster_sync();  // barriers of both CTAs initialised, TMEM allocated
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const long long budget = P.wait_budget;
@@ -224,79 +150,82 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
+      // Both CTAs load their own halves (A rows, B columns) into their own
+      // shared memory; completion is counted on the leader's full barrier.
       for (int c = 0; c < P.n_classes; ++c) {
         ptx::prefetch_tmap(&P.cls[c].tmA);
         ptx::prefetch_tmap(&P.cls[c].tmB);
+        ptx::prefetch_tmap(&P.cls[c].tmAux);
+        ptx::prefetch_tmap(&P.cls[c].tmOut);
+        ptx::prefetch_tmap(&P.cls[c].tmOutT);
       }
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t issued_phase[kStages];
-      bool issued[kStages];
-      for (int s = 0; s < kStages; ++s) issued[s] = false, issued_phase[s] = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < P.total_tiles; t += gridDim.x) {
+      const int half = static_cast<int>(rank) * (kBM / 2);
+      for (int t = pair; ok && t < P.total_tiles; t += npairs) {
         const Tile tl = decode_tile<MODE>(P, t);
         const GemmClass& C = P.cls[tl.cls];
         const int kblocks = (C.K + kBK - 1) / kBK;
         for (int kb = 0; kb < kblocks; ++kb) {
+          const long long w0 = prof ? clock64() : 0;
           if (!ptx::mbar_wait(ptx::smem_addr(&empty[stage]), phase ^ 1, budget, abort)) {
             raise_timeout(P, abort);
             ok = false;
             break;
           }
-          const uint32_t fb = ptx::smem_addr(&full[stage]);
+          if (prof) prof[kWpProducerEmpty] += clock64() - w0;
+          const uint32_t fb = ptx::map_to_rank(ptx::smem_addr(&full[stage]), 0);
           const uint32_t sa = ptx::smem_addr(smem + stage * kStageBytes);
           const uint32_t sb = sa + kStageA;
-          ptx::mbar_arrive_expect_tx(fb, kStageBytes);
-          ptx::tma_load_3d(sa, &C.tmA, fb, kb * kBK, tl.I * kBM, tl.idx);
+          if (rank == 0) ptx::mbar_arrive_expect_tx(ptx::smem_addr(&full[stage]), 2 * kStageBytes);
+          ptx::tma_load_3d_pair(sa, &C.tmA, fb, kb * kBK, tl.I * kBM + half, tl.idx);
           if (MODE == kUpdate) {
 #pragma unroll
-            for (int j = 0; j < kBN / 64; ++j)
-              ptx::tma_load_3d(sb + j * (64 * kBK * 2), &C.tmB, fb, tl.J * kBN + 64 * j, kb * kBK, tl.idx);
+            for (int j = 0; j < (kBN / 2) / 64; ++j)
+              ptx::tma_load_3d_pair(sb + j * (64 * kBK * 2), &C.tmB, fb, tl.J * kBN + half + 64 * j, kb * kBK,
+                                    tl.idx);
           } else {
-            ptx::tma_load_3d(sb, &C.tmB, fb, kb * kBK, tl.J * kBN, tl.idx);
-            ptx::tma_load_3d(sb + kBM * kBK * 2, &C.tmB, fb, kb * kBK, tl.J * kBN + kBM, tl.idx);
+            ptx::tma_load_3d_pair(sb, &C.tmB, fb, kb * kBK, tl.J * kBN + half, tl.idx);
           }
-          issued[stage] = true;
-          issued_phase[stage] = phase;
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
           }
         }
       }
-      if (!ok) {
-        // let copies already in flight land before the CTA goes away
-        for (int s = 0; s < kStages; ++s)
-          if (issued[s]) ptx::mbar_wait(ptx::smem_addr(&full[s]), issued_phase[s], budget, never);
-      }
     }
   } else if (warp == 1) {
-    if (lane == 0 && !P.inject_stall) {
+    if (lane == 0 && rank == 0 && !P.inject_stall) {
       // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc = ptx::idesc_bf16(kBM, kBN, 0, MODE == kUpdate ? 1 : 0);
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < P.total_tiles; t += gridDim.x, ++it) {
+      const long long loop0 = prof ? clock64() : 0;
+      for (int t = pair; ok && t < P.total_tiles; t += npairs, ++it) {
         const Tile tl = decode_tile<MODE>(P, t);
         const GemmClass& C = P.cls[tl.cls];
         const int kblocks = (C.K + kBK - 1) / kBK;
         const int acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
-        if (!ptx::mbar_wait(ptx::smem_addr(&tempty[acc]), acc_phase ^ 1, budget, abort)) {
+        const long long w1 = prof ? clock64() : 0;
+        if (!ptx::mbar_wait_cluster(ptx::smem_addr(&tempty[acc]), acc_phase ^ 1, budget, abort)) {
           raise_timeout(P, abort);
           break;
         }
+        if (prof) prof[kWpMmaTempty] += clock64() - w1;
         ptx::tc_fence_after();
         const uint32_t d = tmem_base + acc * kBN;
         for (int kb = 0; kb < kblocks; ++kb) {
+          const long long w2 = prof ? clock64() : 0;
           if (!ptx::mbar_wait(ptx::smem_addr(&full[stage]), phase, budget, abort)) {
             raise_timeout(P, abort);
             ok = false;
             break;
           }
+          if (prof) prof[kWpMmaFull] += clock64() - w2;
           ptx::tc_fence_after();
           const uint32_t sa = ptx::smem_addr(smem + stage * kStageBytes);
           const uint32_t sb = sa + kStageA;
@@ -305,82 +234,189 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
             const uint64_t adesc = ptx::sdesc_sw128(sa + k * 32, 16, 1024);
             const uint64_t bdesc = MODE == kUpdate ? ptx::sdesc_sw128(sb + k * 2048, 64 * kBK * 2, 1024)
                                                    : ptx::sdesc_sw128(sb + k * 32, 16, 1024);
-            ptx::mma_bf16(d, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
+            ptx::mma_bf16_pair(d, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
           }
-          ptx::mma_commit(ptx::smem_addr(&empty[stage]));
+          ptx::mma_commit_pair_mc(ptx::smem_addr(&empty[stage]), 0x3);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        ptx::mma_commit(ptx::smem_addr(&tfull[acc]));
+        ptx::mma_commit_pair_mc(ptx::smem_addr(&tfull[acc]), 0x3);
       }
       // wait until every MMA issued here has completed
-      ptx::mma_commit(ptx::smem_addr(drain));
+      ptx::mma_commit_pair(ptx::smem_addr(drain));
       ptx::mbar_wait(ptx::smem_addr(drain), 0, budget, never);
+      if (prof) prof[kWpMmaLoop] += clock64() - loop0;
     }
   } else {
     // -------------------------------------------------------------- epilogue
-    // Warp w (2..9) reads TMEM lane quarter w % 4 (rows 32q..32q+31 of the
-    // tile) and the column half (w - 2) / 4 (chunks 4h .. 4h+3 of 32 columns).
+    // This CTA's TMEM lanes hold rows 128*rank .. 128*rank+127 of the 256-row
+    // tile.  Warp w (2..9) reads lane quarter w % 4 (32 rows) and column half
+    // (w - 2) / 4 (4 chunks of 32 columns).  The tile's 128 x 256 bf16 block
+    // goes through the staging buffer: the epilogue input (A or X) arrives
+    // there by TMA, each thread reads its row's 16-byte pieces, writes the
+    // result in place, and one thread stores the block with TMA.  Gram and
+    // polynomial tiles above the diagonal also store the transposed block.
+    // The layout is TMA's 128-byte swizzle: boxes of 64 columns, rows of
+    // 128 bytes, 16-byte piece j of row r at piece (j ^ (r % 8)).
     const int q = warp & 3;
-    const int half = (warp - 2) >> 2;
-    const int row_in_tile = q * 32 + lane;
+    const int colhalf = (warp - 2) >> 2;
+    const int row_local = q * 32 + lane;  // 0 .. 127 within this CTA's rows
+    const bool elected = warp == 2 && lane == 0;
+    const uint32_t stg_a = ptx::smem_addr(stg);
+    const uint32_t tempty_leader[2] = {ptx::map_to_rank(ptx::smem_addr(&tempty[0]), 0),
+                                       ptx::map_to_rank(ptx::smem_addr(&tempty[1]), 0)};
+    const int rowoff = static_cast<int>(rank) * (kBM / 2);
+    auto load_aux = [&](int t) {
+      const Tile tn = decode_tile<MODE>(P, t);
+      const GemmClass& Cn = P.cls[tn.cls];
+      ptx::mbar_arrive_expect_tx(ptx::smem_addr(aux_full), kStageOut);
+#pragma unroll
+      for (int bx = 0; bx < kBN / 64; ++bx)
+        ptx::tma_load_3d(stg_a + bx * (kBM / 2) * 128, &Cn.tmAux, ptx::smem_addr(aux_full), tn.J * kBN + 64 * bx,
+                         tn.I * kBM + rowoff, tn.idx);
+    };
+    if (MODE != kGram && elected && pair < P.total_tiles) load_aux(pair);
+    uint32_t aux_phase = 0;
+    bool ok = true;
     int it = 0;
-    for (int t = blockIdx.x; t < P.total_tiles; t += gridDim.x, ++it) {
+    for (int t = pair; t < P.total_tiles; t += npairs, ++it) {
       const Tile tl = decode_tile<MODE>(P, t);
       const GemmClass& C = P.cls[tl.cls];
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
-      const int rg = tl.I * kBM + row_in_tile;
-      const int warp_row0 = tl.I * kBM + q * 32;
-      const int ncols = MODE == kUpdate ? C.n : C.m;
-      const int cbase = tl.J * kBN + half * (kBN / 2);
-      // this thread's epilogue input for its 128 columns, loaded before the
-      // accumulator is ready so that the loads overlap the main loop
-      uint32_t aux[4][16];
       if (MODE != kGram) {
-        const __nv_bfloat16* arow = C.aux + tl.idx * C.aux_mat_stride + static_cast<long long>(rg) * C.ld_aux;
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          const int c0 = cbase + ch * 32;
-          if (rg < C.m && c0 < ncols) {
-            load_words32(arow + c0, ncols - c0, aux[ch]);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) aux[ch][j] = 0u;
-          }
+        if (!ptx::mbar_wait(ptx::smem_addr(aux_full), aux_phase, budget, abort)) {
+          raise_timeout(P, abort);
+          ok = false;
         }
+        aux_phase ^= 1;
       }
-      if (!ptx::mbar_wait(ptx::smem_addr(&tfull[acc]), acc_phase, budget, abort)) {
+      const long long w3 = (prof && elected) ? clock64() : 0;
+      if (ok && !ptx::mbar_wait(ptx::smem_addr(&tfull[acc]), acc_phase, budget, abort)) {
         raise_timeout(P, abort);
-        break;
+        ok = false;
       }
+      // all epilogue threads must agree on leaving (named barriers follow)
+      if (ptx::named_sync_or(1, 32 * kEpiWarps, !ok || *abort)) break;
+      const long long w4 = (prof && elected) ? clock64() : 0;
+      if (prof && elected) prof[kWpEpiTfull] += w4 - w3;
       ptx::tc_fence_after();
-      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN + half * (kBN / 2);
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN + colhalf * (kBN / 2);
+      uint32_t w[4][16];
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
-        const int c0 = cbase + ch * 32;
-        if (c0 >= ncols) break;  // warp-uniform
-        if (MODE != kUpdate && c0 + 31 < warp_row0) continue;  // strictly below the diagonal
         uint32_t r[32];
         __syncwarp();
         ptx::tmem_ld32(tb + ch * 32, r);
         ptx::tmem_ld_wait();
-        if (rg < C.m) epilogue_chunk<MODE>(P, C, tl, rg, c0, r, aux[ch]);
+        const int c0 = colhalf * (kBN / 2) + ch * 32;  // column within the tile
+        const uint32_t rowa = stg_a + (c0 >> 6) * ((kBM / 2) * 128) + row_local * 128;
+        const int j0 = (c0 & 63) >> 3;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const uint32_t addr = rowa + ((((j0 + jj) ^ (row_local & 7))) << 4);
+          float v[8];
+          if (MODE == kGram) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(r[8 * jj + e]);
+          } else {
+            uint32_t x[4];
+            ptx::lds128(addr, x[0], x[1], x[2], x[3]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float lo = word_lo(x[e]), hi = word_hi(x[e]);
+              const float a0 = __uint_as_float(r[8 * jj + 2 * e]), a1 = __uint_as_float(r[8 * jj + 2 * e + 1]);
+              if (MODE == kPoly) {
+                v[2 * e] = fmaf(P.cb, lo, P.cc * a0);      // b A + c (A A)
+                v[2 * e + 1] = fmaf(P.cb, hi, P.cc * a1);
+              } else {
+                v[2 * e] = fmaf(P.ca, lo, a0);             // a X + B X
+                v[2 * e + 1] = fmaf(P.ca, hi, a1);
+              }
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) w[ch][4 * jj + e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
+          ptx::sts128(addr, w[ch][4 * jj], w[ch][4 * jj + 1], w[ch][4 * jj + 2], w[ch][4 * jj + 3]);
+        }
       }
+      // accumulator drained: the MMA warp may reuse it
       ptx::tc_fence_before();
-      ptx::mbar_arrive(ptx::smem_addr(&tempty[acc]));
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(tempty_leader[acc]);
+      ptx::fence_async_smem();
+      ptx::named_sync(1, 32 * kEpiWarps);
+      if (elected) {
+#pragma unroll
+        for (int bx = 0; bx < kBN / 64; ++bx)
+          ptx::tma_store_3d(&C.tmOut, stg_a + bx * (kBM / 2) * 128, tl.J * kBN + 64 * bx, tl.I * kBM + rowoff,
+                            tl.idx);
+        ptx::bulk_commit();
+      }
+      if (MODE != kUpdate && tl.I != tl.J) {
+        // mirrored block: rows J*256 .. +255, columns of this CTA's rows;
+        // staged as 2 boxes of 256 rows x 64 columns
+        if (elected) ptx::bulk_wait_read0();
+        ptx::named_sync(1, 32 * kEpiWarps);
+        const uint32_t boxa = stg_a + (row_local >> 6) * (kBN * 128);
+        const int jr = (row_local & 63) >> 3;
+        const uint32_t within = (row_local & 7) * 2;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int cl = colhalf * (kBN / 2) + ch * 32 + j;  // mirrored row within the block
+            const uint32_t addr = boxa + cl * 128 + (((jr ^ (cl & 7))) << 4) + within;
+            ptx::sts16(addr, static_cast<uint16_t>((w[ch][j >> 1] >> (16 * (j & 1))) & 0xFFFFu));
+          }
+        }
+        ptx::fence_async_smem();
+        ptx::named_sync(1, 32 * kEpiWarps);
+        if (elected) {
+#pragma unroll
+          for (int bx = 0; bx < (kBM / 2) / 64; ++bx)
+            ptx::tma_store_3d(&C.tmOutT, stg_a + bx * (kBN * 128), tl.I * kBM + rowoff + 64 * bx, tl.J * kBN,
+                              tl.idx);
+          ptx::bulk_commit();
+        }
+      }
+      if (elected) {
+        ptx::bulk_wait_read0();  // staging free again
+        if (MODE != kGram && t + npairs < P.total_tiles) {
+          ptx::fence_async_smem();
+          load_aux(t + npairs);
+        }
+      }
+      ptx::named_sync(1, 32 * kEpiWarps);
+      if (prof && elected) {
+        prof[kWpEpiBusy] += clock64() - w4;
+        prof[kWpTiles] += 1;
+      }
+    }
+    if (elected) ptx::bulk_wait0();
+    if (MODE != kGram && elected && *abort) {
+      // an input tile may still be in flight
+      ptx::mbar_wait(ptx::smem_addr(aux_full), aux_phase, budget, never);
     }
   }
 
   ptx::tc_fence_before();
-  __syncthreads();
+  if (*abort) {
+    // give copies this CTA issued before giving up time to land
+    const long long t0 = clock64();
+    while (clock64() - t0 < 200000) {
+    }
+  }
+  __syncwarp();
+  ptx::cluster_sync();
+  if (prof && threadIdx.x == 0) prof[kWpKernel] += clock64() - t_start;
   if (warp == 1) {
     __syncwarp();
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, 512);
+    ptx::tmem_dealloc_pair(tmem_base, 512);
   }
 }
 
@@ -389,16 +425,39 @@ template __global__ void ns_gemm_kernel<kPoly>(const __grid_constant__ GemmParam
 template __global__ void ns_gemm_kernel<kUpdate>(const __grid_constant__ GemmParams P);
 
 // ------------------------------------------------------------------ launcher
+// Clusters of two CTAs (one pair per cluster), persistent: as many pairs as
+// can be resident at once, at most one per tile.
 cudaError_t launch_ns_gemm(int mode, const GemmParams& P, int num_sms, cudaStream_t stream) {
   const void* fn = mode == kGram   ? reinterpret_cast<const void*>(&ns_gemm_kernel<kGram>)
                    : mode == kPoly ? reinterpret_cast<const void*>(&ns_gemm_kernel<kPoly>)
                                    : reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate>);
+  static int max_pairs[3] = {0, 0, 0};
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
   if (e != cudaSuccess) return e;
-  const int grid = P.total_tiles < num_sms ? P.total_tiles : num_sms;
-  if (grid <= 0) return cudaSuccess;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = kGemmSmem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (max_pairs[mode] <= 0) {
+    cfg.gridDim = dim3(num_sms);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+    if (e != cudaSuccess) return e;
+    max_pairs[mode] = n > 0 ? n : 1;
+  }
+  int pairs = max_pairs[mode] < num_sms / 2 ? max_pairs[mode] : num_sms / 2;
+  if (P.total_tiles < pairs) pairs = P.total_tiles;
+  if (pairs <= 0) return cudaSuccess;
+  cfg.gridDim = dim3(2 * pairs);
   void* args[] = {const_cast<GemmParams*>(&P)};
-  return cudaLaunchKernel(fn, dim3(grid), dim3(kGemmThreads), args, kGemmSmem, stream);
+  return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 }  // namespace muon

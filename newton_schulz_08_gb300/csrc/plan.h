@@ -84,11 +84,9 @@ struct GemmClass {
   CUtensorMap tmA;              // operand A (K-major rows, box 64 x 128)
   CUtensorMap tmB;              // operand B (Gram/poly: K-major box 64 x 128;
                                 //            update: MN-major box 64 x 64)
-  __nv_bfloat16* out;           // output region (A, B or X_{t+1})
-  const __nv_bfloat16* aux;     // epilogue input (A for poly, X_t for update)
-  long long out_mat_stride;     // elements between matrices of out
-  long long aux_mat_stride;
-  int ld_out, ld_aux;
+  CUtensorMap tmAux;            // epilogue input tile (A or X_t), box 64 x 128
+  CUtensorMap tmOut;            // output tile, box 64 x 128
+  CUtensorMap tmOutT;           // mirrored output block (Gram/poly), box 64 x 256
   int m, n, count, K;
   int tiles_m, tiles_n, tiles_per_mat;
   int tile_begin;
@@ -105,6 +103,20 @@ struct GemmParams {
   long long wait_budget;        // clock64 cycles per barrier wait
   int inject_stall;             // test hook: MMA warp issues nothing
   int pad;
+  long long* wait_profile;      // diagnostics: kWaitCounters per CTA, or null
+};
+
+// diagnostics counters per CTA (clock64 cycles unless noted)
+enum WaitCounter {
+  kWpProducerEmpty = 0,  // producer waiting for a free stage
+  kWpMmaFull,            // MMA issuer waiting for operands
+  kWpMmaTempty,          // MMA issuer waiting for a drained accumulator
+  kWpEpiTfull,           // epilogue (warp 2) waiting for an accumulator
+  kWpEpiBusy,            // epilogue (warp 2) working on tiles
+  kWpKernel,             // thread 0: whole kernel
+  kWpTiles,              // tiles processed (count)
+  kWpMmaLoop,            // MMA issuer: whole loop
+  kWaitCounters
 };
 
 // ---------------------------------------------------------------- apply
@@ -126,15 +138,17 @@ struct ApplyParams {
   const MatInfo* table;
 };
 
-// tile sizes of the tcgen05 kernels
-constexpr int kBM = 128;
+// tile sizes of the tcgen05 kernels: a CTA pair computes a kBM x kBN tile,
+// each CTA holding half of the A rows and half of the B columns
+constexpr int kBM = 256;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
-constexpr int kStages = 4;
-constexpr int kStageA = kBM * kBK * 2;        // 16 KB
-constexpr int kStageB = kBN * kBK * 2;        // 32 KB
+constexpr int kStages = 5;
+constexpr int kStageA = (kBM / 2) * kBK * 2;  // 16 KB
+constexpr int kStageB = (kBN / 2) * kBK * 2;  // 16 KB
 constexpr int kStageBytes = kStageA + kStageB;
-constexpr int kGemmSmem = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int kStageOut = (kBM / 2) * kBN * 2;  // 64 KB epilogue staging
+constexpr int kGemmSmem = kStages * kStageBytes + kStageOut + 1024 /*align*/ + 256 /*barriers*/;
 constexpr int kEpiWarps = 8;     // two warps per TMEM lane quarter, one per column half
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 
