@@ -26,6 +26,28 @@ namespace {
 
 constexpr int kEwThreads = 256;
 
+// Programmatic dependent launch: wait for the previous grid's results, then
+// let the next grid be scheduled.
+__device__ __forceinline__ void ptx_grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+cudaError_t launch_pdl(const void* fn, int blocks, void** args, cudaStream_t stream) {
+  if (blocks <= 0) return cudaSuccess;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(kEwThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
 __device__ __forceinline__ float bf16_round(float x) {
   return __bfloat162float(__float2bfloat16_rn(x));
 }
@@ -60,6 +82,7 @@ __device__ __forceinline__ float momentum_u(float g, float* buf, long long i, fl
 }  // namespace
 
 __global__ void __launch_bounds__(kEwThreads) momentum_cast_kernel(const __grid_constant__ K1Params P) {
+  ptx_grid_dep_wait();
   __shared__ float red[kEwThreads / 32];
   __shared__ float tile[64][65];
   // which matrix: largest i with block_begin[i] <= blockIdx.x
@@ -245,6 +268,7 @@ __global__ void __launch_bounds__(kEwThreads) momentum_cast_kernel(const __grid_
 }
 
 __global__ void __launch_bounds__(kEwThreads) normalise_kernel(const __grid_constant__ NormParams P) {
+  ptx_grid_dep_wait();
   __shared__ float red[kEwThreads / 32];
   __shared__ float sh_d;
   int c = 0;
@@ -306,6 +330,7 @@ __global__ void __launch_bounds__(kEwThreads) normalise_kernel(const __grid_cons
 // tile so that both the reads of X and the accesses to p / O are contiguous
 // across a warp.
 __global__ void __launch_bounds__(kEwThreads) apply_kernel(const __grid_constant__ ApplyParams P) {
+  ptx_grid_dep_wait();
   __shared__ float tile[64][65];
   int c = 0;
   while (c + 1 < P.n_classes && (int)blockIdx.x >= P.cls[c + 1].tile_begin) ++c;
@@ -386,24 +411,18 @@ __global__ void __launch_bounds__(kEwThreads) apply_kernel(const __grid_constant
 }
 
 cudaError_t launch_momentum_cast(const K1Params& P, int blocks, cudaStream_t stream) {
-  if (blocks <= 0) return cudaSuccess;
   void* args[] = {const_cast<K1Params*>(&P)};
-  return cudaLaunchKernel(reinterpret_cast<const void*>(&momentum_cast_kernel), dim3(blocks),
-                          dim3(kEwThreads), args, 0, stream);
+  return launch_pdl(reinterpret_cast<const void*>(&momentum_cast_kernel), blocks, args, stream);
 }
 
 cudaError_t launch_apply(const ApplyParams& P, int blocks, cudaStream_t stream) {
-  if (blocks <= 0) return cudaSuccess;
   void* args[] = {const_cast<ApplyParams*>(&P)};
-  return cudaLaunchKernel(reinterpret_cast<const void*>(&apply_kernel), dim3(blocks), dim3(kEwThreads), args,
-                          0, stream);
+  return launch_pdl(reinterpret_cast<const void*>(&apply_kernel), blocks, args, stream);
 }
 
 cudaError_t launch_normalise(const NormParams& P, int blocks, cudaStream_t stream) {
-  if (blocks <= 0) return cudaSuccess;
   void* args[] = {const_cast<NormParams*>(&P)};
-  return cudaLaunchKernel(reinterpret_cast<const void*>(&normalise_kernel), dim3(blocks),
-                          dim3(kEwThreads), args, 0, stream);
+  return launch_pdl(reinterpret_cast<const void*>(&normalise_kernel), blocks, args, stream);
 }
 
 }  // namespace muon

@@ -401,6 +401,9 @@ muon_status_t run(const std::vector<JobMat>& mats, const Plan& P, float lr, floa
             g.K = cp.m;
           }
           if (!ok) return MUON_ERR_CUDA;
+          g.out = static_cast<__nv_bfloat16*>(mode == kGram ? A : B);
+          g.ld_out = cp.lda;
+          g.out_mat_stride = static_cast<long long>(cp.m) * cp.lda;
           g.m = cp.m;
           g.n = cp.n;
           g.count = cp.count;

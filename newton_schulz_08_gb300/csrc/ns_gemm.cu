@@ -144,6 +144,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   __syncwarp();
   ptx::cluster_sync();  // barriers of both CTAs initialised, TMEM allocated
   ptx::tc_fence_after();
+  // the prologue above overlaps the previous kernel's tail; from here on this
+  // kernel reads what that kernel wrote
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   const uint32_t tmem_base = *tmem_slot;
   const long long budget = P.wait_budget;
 
@@ -258,7 +262,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     // goes through the staging buffer: the epilogue input (A or X) arrives
     // there by TMA, each thread reads its row's 16-byte pieces, writes the
     // result in place, and one thread stores the block with TMA.  Gram and
-    // polynomial tiles above the diagonal also store the transposed block.
+    // polynomial tiles above the diagonal also write their mirrored entries
+    // from registers, coalesced across the warp.
     // The layout is TMA's 128-byte swizzle: boxes of 64 columns, rows of
     // 128 bytes, 16-byte piece j of row r at piece (j ^ (r % 8)).
     const int q = warp & 3;
@@ -357,30 +362,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         ptx::bulk_commit();
       }
       if (MODE != kUpdate && tl.I != tl.J) {
-        // mirrored block: rows J*256 .. +255, columns of this CTA's rows;
-        // staged as 2 boxes of 256 rows x 64 columns
-        if (elected) ptx::bulk_wait_read0();
-        ptx::named_sync(1, 32 * kEpiWarps);
-        const uint32_t boxa = stg_a + (row_local >> 6) * (kBN * 128);
-        const int jr = (row_local & 63) >> 3;
-        const uint32_t within = (row_local & 7) * 2;
+        // mirrored entries (r, c) -> (c, r), straight from registers: a warp
+        // writes 32 adjacent r of one row c (64 contiguous bytes) per store
+        const int rg = tl.I * kBM + rowoff + row_local;
+        if (rg < C.m) {
+          uint16_t* mcol = reinterpret_cast<uint16_t*>(C.out + tl.idx * C.out_mat_stride) + rg;
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
+          for (int ch = 0; ch < 4; ++ch) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int cl = colhalf * (kBN / 2) + ch * 32 + j;  // mirrored row within the block
-            const uint32_t addr = boxa + cl * 128 + (((jr ^ (cl & 7))) << 4) + within;
-            ptx::sts16(addr, static_cast<uint16_t>((w[ch][j >> 1] >> (16 * (j & 1))) & 0xFFFFu));
+            for (int j = 0; j < 32; ++j) {
+              const int c = tl.J * kBN + colhalf * (kBN / 2) + ch * 32 + j;
+              if (c < C.m)
+                mcol[static_cast<long long>(c) * C.ld_out] =
+                    static_cast<uint16_t>((w[ch][j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+            }
           }
-        }
-        ptx::fence_async_smem();
-        ptx::named_sync(1, 32 * kEpiWarps);
-        if (elected) {
-#pragma unroll
-          for (int bx = 0; bx < (kBM / 2) / 64; ++bx)
-            ptx::tma_store_3d(&C.tmOutT, stg_a + bx * (kBN * 128), tl.I * kBM + rowoff + 64 * bx, tl.J * kBN,
-                              tl.idx);
-          ptx::bulk_commit();
         }
       }
       if (elected) {
@@ -432,13 +428,18 @@ cudaError_t launch_ns_gemm(int mode, const GemmParams& P, int num_sms, cudaStrea
                    : mode == kPoly ? reinterpret_cast<const void*>(&ns_gemm_kernel<kPoly>)
                                    : reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate>);
   static int max_pairs[3] = {0, 0, 0};
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
-  if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
+  cudaError_t e = cudaSuccess;
+  if (max_pairs[mode] <= 0) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kGemmThreads);
   cfg.dynamicSmemBytes = kGemmSmem;
@@ -456,6 +457,7 @@ cudaError_t launch_ns_gemm(int mode, const GemmParams& P, int num_sms, cudaStrea
   if (P.total_tiles < pairs) pairs = P.total_tiles;
   if (pairs <= 0) return cudaSuccess;
   cfg.gridDim = dim3(2 * pairs);
+  cfg.numAttrs = 2;
   void* args[] = {const_cast<GemmParams*>(&P)};
   return cudaLaunchKernelExC(&cfg, fn, args);
 }

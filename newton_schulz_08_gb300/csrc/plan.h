@@ -86,7 +86,10 @@ struct GemmClass {
                                 //            update: MN-major box 64 x 64)
   CUtensorMap tmAux;            // epilogue input tile (A or X_t), box 64 x 128
   CUtensorMap tmOut;            // output tile, box 64 x 128
-  CUtensorMap tmOutT;           // mirrored output block (Gram/poly), box 64 x 256
+  CUtensorMap tmOutT;           // unused (kept for layout)
+  __nv_bfloat16* out;           // output region (mirrored writes of Gram/poly)
+  long long out_mat_stride;     // elements between matrices of out
+  int ld_out;
   int m, n, count, K;
   int tiles_m, tiles_n, tiles_per_mat;
   int tile_begin;
