@@ -116,52 +116,70 @@ __global__ void __launch_bounds__(kEwThreads) momentum_cast_kernel(const __grid_
     if (vec) {
       const int cv = C >> 3;  // 8-element vectors per row
       const long long nvec = static_cast<long long>(r1 - r0) * cv;
-      for (long long v = threadIdx.x; v < nvec; v += kEwThreads) {
-        const int r = r0 + static_cast<int>(v / cv);
-        const int c = static_cast<int>(v % cv) * 8;
-        const long long i = static_cast<long long>(r) * C + c;
-        float g[8];
-        if (M.g_f32) {
-          const float4* gp = reinterpret_cast<const float4*>(static_cast<const float*>(M.g) + i);
-          const float4 a = gp[0], bq = gp[1];
-          g[0] = a.x; g[1] = a.y; g[2] = a.z; g[3] = a.w;
-          g[4] = bq.x; g[5] = bq.y; g[6] = bq.z; g[7] = bq.w;
-        } else {
-          const uint4 w = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(M.g) + i);
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+      // two vectors per thread per iteration, all loads issued before any
+      // store so that both are in flight together
+      for (long long v0 = threadIdx.x; v0 < nvec; v0 += 2 * kEwThreads) {
+        float g[2][8], bv[2][8];
+        long long iv[2];
+        bool have[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const long long v = v0 + h * kEwThreads;
+          have[h] = v < nvec;
+          const int r = r0 + static_cast<int>((have[h] ? v : v0) / cv);
+          const int c = static_cast<int>((have[h] ? v : v0) % cv) * 8;
+          iv[h] = static_cast<long long>(r) * C + c;
+          if (!have[h]) continue;
+          if (M.g_f32) {
+            const float4* gp = reinterpret_cast<const float4*>(static_cast<const float*>(M.g) + iv[h]);
+            const float4 a = gp[0], bq = gp[1];
+            g[h][0] = a.x; g[h][1] = a.y; g[h][2] = a.z; g[h][3] = a.w;
+            g[h][4] = bq.x; g[h][5] = bq.y; g[h][6] = bq.z; g[h][7] = bq.w;
+          } else {
+            const uint4 w = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(M.g) + iv[h]);
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              g[h][2 * k] = __uint_as_float(ws[k] << 16);
+              g[h][2 * k + 1] = __uint_as_float(ws[k] & 0xFFFF0000u);
+            }
+          }
+          if (M.buf) {
+            const float4* bp = reinterpret_cast<const float4*>(M.buf + iv[h]);
+            const float4 b0 = bp[0], b1 = bp[1];
+            bv[h][0] = b0.x; bv[h][1] = b0.y; bv[h][2] = b0.z; bv[h][3] = b0.w;
+            bv[h][4] = b1.x; bv[h][5] = b1.y; bv[h][6] = b1.z; bv[h][7] = b1.w;
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (!have[h]) continue;
+          float u[8];
+          if (M.buf) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              bv[h][k] = fmaf(P.mu, bv[h][k], g[h][k]);
+              u[k] = P.nesterov ? fmaf(P.mu, bv[h][k], g[h][k]) : bv[h][k];
+            }
+            float4* bp = reinterpret_cast<float4*>(M.buf + iv[h]);
+            bp[0] = make_float4(bv[h][0], bv[h][1], bv[h][2], bv[h][3]);
+            bp[1] = make_float4(bv[h][4], bv[h][5], bv[h][6], bv[h][7]);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) u[k] = g[h][k];
+          }
+          uint32_t packed[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            g[2 * k] = __uint_as_float(ws[k] << 16);
-            g[2 * k + 1] = __uint_as_float(ws[k] & 0xFFFF0000u);
+            const __nv_bfloat162 hh = __floats2bfloat162_rn(u[2 * k], u[2 * k + 1]);
+            packed[k] = *reinterpret_cast<const uint32_t*>(&hh);
+            const float x0 = __low2float(hh), x1 = __high2float(hh);
+            ss = fmaf(x0, x0, ss);
+            ss = fmaf(x1, x1, ss);
           }
+          const long long r = iv[h] / C, c = iv[h] % C;
+          *reinterpret_cast<uint4*>(M.x + r * M.ldx + c) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
         }
-        float u[8];
-        if (M.buf) {
-          float4* bp = reinterpret_cast<float4*>(M.buf + i);
-          float4 b0 = bp[0], b1 = bp[1];
-          float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            bv[k] = fmaf(P.mu, bv[k], g[k]);
-            u[k] = P.nesterov ? fmaf(P.mu, bv[k], g[k]) : bv[k];
-          }
-          bp[0] = make_float4(bv[0], bv[1], bv[2], bv[3]);
-          bp[1] = make_float4(bv[4], bv[5], bv[6], bv[7]);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) u[k] = g[k];
-        }
-        uint32_t packed[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const __nv_bfloat162 h = __floats2bfloat162_rn(u[2 * k], u[2 * k + 1]);
-          packed[k] = *reinterpret_cast<const uint32_t*>(&h);
-          const float x0 = __low2float(h), x1 = __high2float(h);
-          ss = fmaf(x0, x0, ss);
-          ss = fmaf(x1, x1, ss);
-        }
-        *reinterpret_cast<uint4*>(M.x + static_cast<long long>(r) * M.ldx + c) =
-            make_uint4(packed[0], packed[1], packed[2], packed[3]);
       }
     } else {
       const long long ne = static_cast<long long>(r1 - r0) * C;
@@ -298,20 +316,33 @@ __global__ void __launch_bounds__(kEwThreads) normalise_kernel(const __grid_cons
   if ((n & 7) == 0) {
     const int cv = n >> 3;
     const long long nvec = static_cast<long long>(r1 - r0) * cv;
-    for (long long v = threadIdx.x; v < nvec; v += kEwThreads) {
-      const int r = r0 + static_cast<int>(v / cv);
-      const int cc = static_cast<int>(v % cv) * 8;
-      uint4* p = reinterpret_cast<uint4*>(X + static_cast<long long>(r) * K.ldx + cc);
-      uint4 w = *p;
-      uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    for (long long v0 = threadIdx.x; v0 < nvec; v0 += 2 * kEwThreads) {
+      uint4* ptr[2];
+      uint4 w[2];
+      bool have[2];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float lo = __uint_as_float(ws[k] << 16) / d;
-        const float hi = __uint_as_float(ws[k] & 0xFFFF0000u) / d;
-        const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-        ws[k] = *reinterpret_cast<const uint32_t*>(&h);
+      for (int h = 0; h < 2; ++h) {
+        const long long v = v0 + h * kEwThreads;
+        have[h] = v < nvec;
+        const long long vv = have[h] ? v : v0;
+        const int r = r0 + static_cast<int>(vv / cv);
+        const int cc = static_cast<int>(vv % cv) * 8;
+        ptr[h] = reinterpret_cast<uint4*>(X + static_cast<long long>(r) * K.ldx + cc);
+        if (have[h]) w[h] = *ptr[h];
       }
-      *p = make_uint4(ws[0], ws[1], ws[2], ws[3]);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (!have[h]) continue;
+        uint32_t ws[4] = {w[h].x, w[h].y, w[h].z, w[h].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float lo = __uint_as_float(ws[k] << 16) / d;
+          const float hi = __uint_as_float(ws[k] & 0xFFFF0000u) / d;
+          const __nv_bfloat162 hh = __floats2bfloat162_rn(lo, hi);
+          ws[k] = *reinterpret_cast<const uint32_t*>(&hh);
+        }
+        *ptr[h] = make_uint4(ws[0], ws[1], ws[2], ws[3]);
+      }
     }
   } else {
     const long long ne = static_cast<long long>(r1 - r0) * n;
@@ -345,22 +376,35 @@ __global__ void __launch_bounds__(kEwThreads) apply_kernel(const __grid_constant
   const __nv_bfloat16* X = K.x + static_cast<long long>(idx) * K.m * K.ldx;
   const int m = K.m, n = K.n;
   const int tid = threadIdx.x;
+  const bool param = P.final_mode == kFinalParam;
   if (!mi.tall) {
     // stored as X: element (r, c) at r * n + c; a thread handles 8 columns
-    // of two rows
+    // of two rows, both rows' loads issued before the stores
+    if ((n & 7) == 0) {
+      uint4 w[2];
+      float4 pa[2], pb[2];
+      long long o[2];
+      bool have[2];
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int r = r0 + (tid >> 3) + 32 * k;
-      const int cc = c0 + (tid & 7) * 8;
-      if (r >= m || cc >= n) continue;
-      const __nv_bfloat16* xs = X + static_cast<long long>(r) * K.ldx + cc;
-      const long long o = static_cast<long long>(r) * n + cc;
-      if ((n & 7) == 0) {
-        const uint4 w = *reinterpret_cast<const uint4*>(xs);
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-        if (P.final_mode == kFinalParam) {
-          float4* pp = reinterpret_cast<float4*>(static_cast<float*>(mi.out) + o);
-          float4 a = pp[0], b = pp[1];
+      for (int k = 0; k < 2; ++k) {
+        const int r = r0 + (tid >> 3) + 32 * k;
+        const int cc = c0 + (tid & 7) * 8;
+        have[k] = r < m && cc < n;
+        o[k] = static_cast<long long>(r) * n + cc;
+        if (!have[k]) continue;
+        w[k] = *reinterpret_cast<const uint4*>(X + static_cast<long long>(r) * K.ldx + cc);
+        if (param) {
+          const float4* pp = reinterpret_cast<const float4*>(static_cast<const float*>(mi.out) + o[k]);
+          pa[k] = pp[0];
+          pb[k] = pp[1];
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        if (!have[k]) continue;
+        if (param) {
+          const uint32_t ws[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+          float4 a = pa[k], b = pb[k];
           a.x = fmaf(-P.lr, __uint_as_float(ws[0] << 16), a.x);
           a.y = fmaf(-P.lr, __uint_as_float(ws[0] & 0xFFFF0000u), a.y);
           a.z = fmaf(-P.lr, __uint_as_float(ws[1] << 16), a.z);
@@ -369,15 +413,24 @@ __global__ void __launch_bounds__(kEwThreads) apply_kernel(const __grid_constant
           b.y = fmaf(-P.lr, __uint_as_float(ws[2] & 0xFFFF0000u), b.y);
           b.z = fmaf(-P.lr, __uint_as_float(ws[3] << 16), b.z);
           b.w = fmaf(-P.lr, __uint_as_float(ws[3] & 0xFFFF0000u), b.w);
+          float4* pp = reinterpret_cast<float4*>(static_cast<float*>(mi.out) + o[k]);
           pp[0] = a;
           pp[1] = b;
         } else {
-          *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(mi.out) + o) = w;
+          *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(mi.out) + o[k]) = w[k];
         }
-      } else {
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int r = r0 + (tid >> 3) + 32 * k;
+        const int cc = c0 + (tid & 7) * 8;
+        if (r >= m || cc >= n) continue;
+        const __nv_bfloat16* xs = X + static_cast<long long>(r) * K.ldx + cc;
+        const long long o = static_cast<long long>(r) * n + cc;
         for (int j = 0; j < 8 && cc + j < n; ++j) {
           const __nv_bfloat16 x = xs[j];
-          if (P.final_mode == kFinalParam) {
+          if (param) {
             float* pp = static_cast<float*>(mi.out) + o + j;
             *pp = fmaf(-P.lr, __bfloat162float(x), *pp);
           } else {
@@ -387,24 +440,75 @@ __global__ void __launch_bounds__(kEwThreads) apply_kernel(const __grid_constant
       }
     }
   } else {
-    // stored as X^T (n x m): element (c, r) at c * m + r
-    for (int e = tid; e < 64 * 64; e += kEwThreads) {
-      const int rr = e >> 6, cc = e & 63;
+    // stored as X^T (n x m): element (c, r) at c * m + r.  X tile in with
+    // 16-byte loads, out along p's rows with 4-element vectors.
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int e = tid + kEwThreads * k;
+      const int rr = e >> 3, cc = (e & 7) * 8;
       const int r = r0 + rr, col = c0 + cc;
-      tile[rr][cc] = (r < m && col < n) ? __bfloat162float(X[static_cast<long long>(r) * K.ldx + col]) : 0.0f;
+      if (r < m && col + 8 <= n) {
+        const uint4 v = *reinterpret_cast<const uint4*>(X + static_cast<long long>(r) * K.ldx + col);
+        const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          tile[rr][cc + 2 * j] = __uint_as_float(ws[j] << 16);
+          tile[rr][cc + 2 * j + 1] = __uint_as_float(ws[j] & 0xFFFF0000u);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          tile[rr][cc + j] = (r < m && col + j < n) ? __bfloat162float(X[static_cast<long long>(r) * K.ldx + col + j]) : 0.0f;
+      }
     }
     __syncthreads();
-    for (int e = tid; e < 64 * 64; e += kEwThreads) {
-      const int cc = e >> 6, rr = e & 63;
-      const int r = r0 + rr, col = c0 + cc;
-      if (r >= m || col >= n) continue;
-      const long long o = static_cast<long long>(col) * m + r;
-      const float x = tile[rr][cc];
-      if (P.final_mode == kFinalParam) {
-        float* pp = static_cast<float*>(mi.out) + o;
-        *pp = fmaf(-P.lr, x, *pp);
-      } else {
-        static_cast<__nv_bfloat16*>(mi.out)[o] = __float2bfloat16_rn(x);
+    if ((m & 3) == 0) {
+      float4 pv[4];
+      bool have[4];
+      long long o[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int e = tid + kEwThreads * k;
+        const int jj = e >> 4, rr = (e & 15) * 4;
+        const int col = c0 + jj, r = r0 + rr;
+        have[k] = col < n && r < m;  // m % 4 == 0: the 4 entries are all in range
+        o[k] = static_cast<long long>(col) * m + r;
+        if (have[k] && param) pv[k] = *reinterpret_cast<const float4*>(static_cast<const float*>(mi.out) + o[k]);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (!have[k]) continue;
+        const int e = tid + kEwThreads * k;
+        const int jj = e >> 4, rr = (e & 15) * 4;
+        const float x0 = tile[rr][jj], x1 = tile[rr + 1][jj], x2 = tile[rr + 2][jj], x3 = tile[rr + 3][jj];
+        if (param) {
+          float4 a = pv[k];
+          a.x = fmaf(-P.lr, x0, a.x);
+          a.y = fmaf(-P.lr, x1, a.y);
+          a.z = fmaf(-P.lr, x2, a.z);
+          a.w = fmaf(-P.lr, x3, a.w);
+          *reinterpret_cast<float4*>(static_cast<float*>(mi.out) + o[k]) = a;
+        } else {
+          const __nv_bfloat162 h0 = __floats2bfloat162_rn(x0, x1), h1 = __floats2bfloat162_rn(x2, x3);
+          uint2 u;
+          u.x = *reinterpret_cast<const uint32_t*>(&h0);
+          u.y = *reinterpret_cast<const uint32_t*>(&h1);
+          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(mi.out) + o[k]) = u;
+        }
+      }
+    } else {
+      for (int e = tid; e < 64 * 64; e += kEwThreads) {
+        const int cc = e >> 6, rr = e & 63;
+        const int r = r0 + rr, col = c0 + cc;
+        if (r >= m || col >= n) continue;
+        const long long o = static_cast<long long>(col) * m + r;
+        const float x = tile[rr][cc];
+        if (param) {
+          float* pp = static_cast<float*>(mi.out) + o;
+          *pp = fmaf(-P.lr, x, *pp);
+        } else {
+          static_cast<__nv_bfloat16*>(mi.out)[o] = __float2bfloat16_rn(x);
+        }
       }
     }
   }
