@@ -50,7 +50,11 @@ def workload_shapes(name):
         "gpt1p5b": inputs.gpt1p5b_shapes(),
         "rect": inputs.rect_shapes(),
         "single": [inputs.SINGLE["shape"]],
+        "spectra": inputs.spectra_shapes(),
     }[name]
+
+
+NS5_ONLY = {"spectra"}
 
 
 WORKLOAD_DESC = {
@@ -60,6 +64,8 @@ WORKLOAD_DESC = {
                "1.4746B fp32 params, bf16 grads, fp32 momentum",
     "rect": "rectangular bank: 8 each of 1024x4096, 4096x1024, 768x3072, 2048x8192, bf16 grads",
     "single": "single 128x512 matrix, fp32 grad",
+    "spectra": "spectra sweep, Newton-Schulz only (ns5_bank): 64 x 1024x1024 and 16 x 4096x4096 bf16 "
+               "G = U diag(s) V^T, s log-uniform in [1e-4, 1]",
 }
 
 
@@ -74,9 +80,13 @@ def ns_flops(shapes, steps=NS_STEPS):
     return {k: v * steps for k, v in f.items()}
 
 
-def hbm_bytes(shapes, gbytes):
+def hbm_bytes(shapes, gbytes, ns5_only=False):
     """Algorithmic bytes of the elementwise passes for one step over the bank."""
     e = float(sum(r * c for r, c in shapes))
+    if ns5_only:
+        return {"momentum_cast": e * (gbytes + 2),       # G r, Xraw w
+                "normalise": e * 4,                      # Xraw r, X0 w
+                "apply": e * (2 + 2)}                    # X r, O w
     return {"momentum_cast": e * (gbytes + 4 + 4 + 2),  # g, buf r/w, Xraw
             "normalise": e * 4,                          # Xraw r, X0 w
             "apply": e * (2 + 4 + 4)}                    # X r, p r/w
@@ -273,23 +283,58 @@ def main():
 
     L = muon.lib()
     shapes = workload_shapes(args.workload)
-    grad_sets = 3
-    P, Bf, Gs, Gs_host = build_bank(shapes, device, grad_sets)
-    Pv, Bv = views(P, shapes), views(Bf, shapes)
-    descs = []
-    for k in range(grad_sets):
-        arr, n = muon._descs(Pv, views(Gs[k], shapes), Bv)
-        descs.append(arr)
     n_mats = len(shapes)
-    ws = muon.new_workspace(L.muon_workspace_size(descs[0], n_mats), device)
-    ws_ptr, ws_bytes = ctypes.c_void_p(ws.data_ptr()), ws.numel()
+    ns5_only = args.workload in NS5_ONLY
     stream = torch.cuda.current_stream(device)
     sptr = ctypes.c_void_p(stream.cuda_stream)
+    if not ns5_only:
+        grad_sets = 3
+        P, Bf, Gs, Gs_host = build_bank(shapes, device, grad_sets)
+        Pv, Bv = views(P, shapes), views(Bf, shapes)
+        descs = []
+        for k in range(grad_sets):
+            arr, n = muon._descs(Pv, views(Gs[k], shapes), Bv)
+            descs.append(arr)
+        ws = muon.new_workspace(L.muon_workspace_size(descs[0], n_mats), device)
+        ws_ptr, ws_bytes = ctypes.c_void_p(ws.data_ptr()), ws.numel()
 
-    def step(k):
-        st = L.muon_step(descs[k % grad_sets], n_mats, LR, MU, 1, NS_STEPS, ws_ptr, ws_bytes, sptr)
-        if st != 0:
-            raise muon.MuonError(st, "muon_step")
+        def step(k, arr=None):
+            st = L.muon_step(descs[k % grad_sets] if arr is None else arr, n_mats, LR, MU, 1, NS_STEPS,
+                             ws_ptr, ws_bytes, sptr)
+            if st != 0:
+                raise muon.MuonError(st, "muon_step")
+
+        in_dev, in_host = Gs[0], Gs_host               # e2e: this step's gradients in
+        out_dev = P                                    # e2e: the updated parameters out
+        e2e_arr = descs[0]
+        gbytes = 2
+    else:
+        from newton_schulz_08_gb300 import inputs
+        total = sum(r * c for r, c in shapes)
+        Gflat = torch.empty(total, dtype=torch.bfloat16, device=device)
+        off = 0
+        for i, (r, c) in enumerate(shapes):
+            Gflat[off:off + r * c].copy_(inputs.spectra_matrix_device(r, i, device, torch.bfloat16).reshape(-1))
+            off += r * c
+        Oflat = torch.empty_like(Gflat)
+        Gv, Ov = views(Gflat, shapes), views(Oflat, shapes)
+        gp = (ctypes.c_void_p * n_mats)(*[g.data_ptr() for g in Gv])
+        op = (ctypes.c_void_p * n_mats)(*[o.data_ptr() for o in Ov])
+        dt = (ctypes.c_int32 * n_mats)(*([muon.MUON_BF16] * n_mats))
+        rows = (ctypes.c_int64 * n_mats)(*[r for r, _ in shapes])
+        cols = (ctypes.c_int64 * n_mats)(*[c for _, c in shapes])
+        ws = muon.new_workspace(L.ns5_bank_workspace_size(rows, cols, n_mats), device)
+        ws_ptr, ws_bytes = ctypes.c_void_p(ws.data_ptr()), ws.numel()
+
+        def step(k, arr=None):
+            st = L.ns5_bank(gp, dt, op, rows, cols, n_mats, NS_STEPS, ws_ptr, ws_bytes, sptr)
+            if st != 0:
+                raise muon.MuonError(st, "ns5_bank")
+
+        in_dev, in_host = Gflat, [Gflat.cpu().pin_memory()]
+        out_dev = Oflat
+        e2e_arr = None
+        gbytes = 2
 
     def barrier():
         torch.cuda.synchronize(device)
@@ -333,17 +378,14 @@ def main():
     muon.muon_set_debug("record_kernel_events", 0)
 
     # ------------------------------------------------------------- e2e
-    Gh_dev = Gs[0]
-    P_host = torch.empty(P.numel(), dtype=torch.float32).pin_memory()
+    out_host = torch.empty(out_dev.numel(), dtype=out_dev.dtype).pin_memory()
     e_steps = max(3, args.steps // 4)
     barrier()
     e0.record(stream)
     for k in range(e_steps):
-        Gh_dev.copy_(Gs_host[k % grad_sets], non_blocking=True)
-        st_ = L.muon_step(descs[0], n_mats, LR, MU, 1, NS_STEPS, ws_ptr, ws_bytes, sptr)
-        if st_ != 0:
-            raise muon.MuonError(st_, "muon_step")
-        P_host.copy_(P, non_blocking=True)
+        in_dev.copy_(in_host[k % len(in_host)], non_blocking=True)
+        step(0, e2e_arr)
+        out_host.copy_(out_dev, non_blocking=True)
     e1.record(stream)
     barrier()
     clk = clocks.stop()
@@ -360,7 +402,7 @@ def main():
     # ------------------------------------------------------------- report
     peaks, peak_src = load_peaks()
     flops = ns_flops(shapes)
-    gbytes = hbm_bytes(shapes, 2)
+    gbytes = hbm_bytes(shapes, gbytes, ns5_only)
     kern = {}
     for kind, (tot_ms, cnt) in ktimes.items():
         if cnt == 0:
@@ -413,13 +455,13 @@ def main():
         "kernels": kern,
         "e2e": {"value": n_mats * world / (e2e_ms * 1e-3), "unit": "matrices/s",
                 "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": int(Gs_host[0].numel() * 2),
-                "d2h_bytes_per_step": int(P_host.numel() * 4)},
+                "h2d_bytes_per_step": int(in_dev.numel() * in_dev.element_size()),
+                "d2h_bytes_per_step": int(out_dev.numel() * out_dev.element_size())},
         "gpu_launches": int(sum(c for _, c in ktimes.values())),
         "gpu_launches_note": "kernels launched in the per-kernel timing pass (same count as the main timed loop)",
         "clocks": clk,
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and not ns5_only:
         n_cpu, t_cpu = oracle_sample(shapes, args.cpu_budget)
         line["cpu_baseline"] = {"value": n_cpu / t_cpu, "unit": "matrices/s", "cores": cpu_threads(),
                                 "kind": "oracle",

@@ -122,3 +122,19 @@ def single():
     g = normal(shape, 1.0, 0)
     p = normal(shape, 0.02, 1)
     return p, g, np.zeros(shape, np.float32)
+
+
+def spectra_matrix_device(n, i, device, dtype=None):
+    """The spectra recipe drawn with torch on `device` (seeded per matrix):
+    U, V from QR of Gaussians with R's diagonal signs folded in, s
+    log-uniform in [1e-4, 1], G = U diag(s) V^T in float32.  Used where
+    host generation of large banks would be too slow (timing runs); the
+    parity tests use spectra_matrix."""
+    import torch
+    g = torch.Generator(device=device).manual_seed(SEED_U + i)
+    Z = torch.randn((2, n, n), generator=g, device=device, dtype=torch.float32)
+    Q, R = torch.linalg.qr(Z)
+    Q = Q * torch.sign(torch.diagonal(R, dim1=-2, dim2=-1)).unsqueeze(-2)
+    s = torch.exp(torch.empty(n, device=device).uniform_(float(np.log(1e-4)), 0.0, generator=g))
+    G = (Q[0] * s) @ Q[1].T
+    return G if dtype is None else G.to(dtype)
