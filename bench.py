@@ -20,8 +20,11 @@ steps, parameter update (18 kernel launches through the C ABI).
              on a bounded sample of the bank's matrices
 
 ``--impl reference`` times the CPU oracle as the reference arm (rank 0 only).
-Multi-GPU (torchrun): every rank updates its own replica of the bank (the
-step does not shard); value = matrices of all ranks / max time over ranks.
+Multi-GPU (torchrun, N ranks): every matrix's step depends on that matrix
+alone, so the units shard with no exchange of data.  The bank is repeated N
+times (weak scaling: one bank's work per GPU) and split between the ranks by
+the library's work-balanced partition (muon_partition); each rank updates the
+matrices it owns.  value = matrices of all ranks / max time over ranks.
 """
 
 import argparse
@@ -221,18 +224,43 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ ranks
+def rank_bank(shapes, world, rank):
+    """The matrices `rank` of `world` processes owns: the bank repeated `world`
+    times (matrix g is shapes[g % len(shapes)]), split by muon.partition.
+    Returns (global ids, shapes); the ids seed each matrix's inputs."""
+    from newton_schulz_08_gb300 import muon
+    full = [shapes[g % len(shapes)] for g in range(len(shapes) * world)]
+    owner = muon.partition(full, world) if world > 1 else [0] * len(full)
+    ids = [g for g, o in enumerate(owner) if o == rank]
+    return ids, [full[g] for g in ids]
+
+
+def max_over_ranks(x, world, device=None):
+    """Largest value of `x` over all ranks (every rank gets it)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ------------------------------------------------------------------ GPU arm
-def build_bank(shapes, device, grad_sets):
-    """Device tensors of the bank: params, bufs, grad sets (flat + views)."""
+def build_bank(shapes, device, grad_sets, ids=None):
+    """Device tensors of the bank: params, bufs, grad sets (flat + views).
+    Matrix k's inputs are seeded by ids[k] (default: k)."""
     import torch
     from newton_schulz_08_gb300 import inputs
+    ids = list(range(len(shapes))) if ids is None else ids
     sizes = [r * c for r, c in shapes]
     total = sum(sizes)
     P = torch.empty(total, dtype=torch.float32, device=device)
     Bf = torch.empty(total, dtype=torch.float32, device=device)
     Gs_host = [torch.empty(total, dtype=torch.bfloat16).pin_memory() for _ in range(grad_sets)]
     off = 0
-    for i, (shape, sz) in enumerate(zip(shapes, sizes)):
+    for i, shape, sz in zip(ids, shapes, sizes):
         P[off:off + sz].copy_(torch.from_numpy(inputs.param(shape, i).ravel()))
         Bf[off:off + sz].copy_(torch.from_numpy(inputs.buffer(shape, i).ravel()))
         for k in range(grad_sets):
@@ -282,14 +310,15 @@ def main():
         dist.init_process_group("nccl", device_id=device)
 
     L = muon.lib()
-    shapes = workload_shapes(args.workload)
+    ids, shapes = rank_bank(workload_shapes(args.workload), world, rank)
     n_mats = len(shapes)
+    n_total = len(workload_shapes(args.workload)) * world
     ns5_only = args.workload in NS5_ONLY
     stream = torch.cuda.current_stream(device)
     sptr = ctypes.c_void_p(stream.cuda_stream)
     if not ns5_only:
         grad_sets = 3
-        P, Bf, Gs, Gs_host = build_bank(shapes, device, grad_sets)
+        P, Bf, Gs, Gs_host = build_bank(shapes, device, grad_sets, ids)
         Pv, Bv = views(P, shapes), views(Bf, shapes)
         descs = []
         for k in range(grad_sets):
@@ -313,7 +342,7 @@ def main():
         total = sum(r * c for r, c in shapes)
         Gflat = torch.empty(total, dtype=torch.bfloat16, device=device)
         off = 0
-        for i, (r, c) in enumerate(shapes):
+        for i, (r, c) in zip(ids, shapes):
             Gflat[off:off + r * c].copy_(inputs.spectra_matrix_device(r, i, device, torch.bfloat16).reshape(-1))
             off += r * c
         Oflat = torch.empty_like(Gflat)
@@ -342,13 +371,6 @@ def main():
             dist.barrier()
         torch.cuda.synchronize(device)
 
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
     for k in range(args.warmup):
         step(k)
     barrier()
@@ -366,7 +388,7 @@ def main():
         step(k)
     e1.record(stream)
     barrier()
-    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, device)
 
     # ---------------------------------------------- per-kernel live timing
     muon.muon_set_debug("record_kernel_events", 1)
@@ -389,7 +411,7 @@ def main():
     e1.record(stream)
     barrier()
     clk = clocks.stop()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, world, device)
     st = muon.muon_device_status(ws)
     if st != 0:
         raise muon.MuonError(st, "device status after timing")
@@ -434,18 +456,19 @@ def main():
         with open(tfile) as f:
             traffic = json.load(f).get(args.workload, {}).get(dom)
 
-    value = n_mats * world / (ms * 1e-3)
+    value = n_total / (ms * 1e-3)
     total_flops = sum(flops.values())
     line = {
         "metric": "muon_step_matrices_per_s", "value": value, "unit": "matrices/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_DESC[args.workload], "matrices": n_mats,
-                   "params": int(sum(r * c for r, c in shapes)), "ns_steps": NS_STEPS,
+        "config": {"workload": WORKLOAD_DESC[args.workload], "matrices": n_total,
+                   "params": int(sum(r * c for r, c in workload_shapes(args.workload))) * world, "ns_steps": NS_STEPS,
                    "lr": LR, "momentum": MU, "nesterov": True,
                    "l2": "no flush: inputs (params, bufs, grads) exceed the 129 MB L2",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": (f"{world} ranks, each owning a work-balanced share of {world} banks "
+                                   "(no data exchanged)" if world > 1 else "1 GPU")},
         "ns5_tflops": total_flops / (ms * 1e-3) / 1e12,
         "ns5_tflops_note": "algorithmic NS FLOPs of the whole step / step time",
         "update_gbs": (gbytes["momentum_cast"] + gbytes["apply"]) / (ms * 1e-3) / 1e9,
@@ -453,7 +476,7 @@ def main():
                      "unit": d["unit"], "frac": d["frac"], "traffic": traffic,
                      "peak_source": f"{peak_src} ({'bf16_tflops burst' if d['unit'] == 'TFLOP/s' else 'hbm_gbs'})"},
         "kernels": kern,
-        "e2e": {"value": n_mats * world / (e2e_ms * 1e-3), "unit": "matrices/s",
+        "e2e": {"value": n_total / (e2e_ms * 1e-3), "unit": "matrices/s",
                 "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": int(in_dev.numel() * in_dev.element_size()),
                 "d2h_bytes_per_step": int(out_dev.numel() * out_dev.element_size())},

@@ -191,6 +191,28 @@ int muon_kernel_times(double* ms, int* launches, int n_kinds);
 muon_status_t ns5_noalloc(const void* G, int g_dtype, void* O, int batch, int64_t rows,
                           int64_t cols, int ns_steps, void* stream);
 
+/* Assigns each matrix of a bank to one of `world` ranks, for running the
+ * step on several GPUs, one process per GPU, each updating only the matrices
+ * it owns (every matrix's step depends on that matrix alone, so no data is
+ * exchanged during the step).  The page's own multi-GPU variant (section
+ * "Muon优化器：动量正交化技术") gives each rank a slice of every size group;
+ * here the split balances the Newton-Schulz work instead: matrices are taken
+ * from the heaviest down (work of an R x C matrix, m = min, n = max:
+ * m(m+1)n + m^2(m+1) + 2 m^2 n) and each goes to the rank with the least work
+ * so far (lowest rank on ties).  Among matrices of equal work, identical
+ * shapes are taken together (more rows first, then more columns, then bank
+ * order), so each shape group is dealt out evenly.  No rank gets more than
+ * one matrix's work above the mean.
+ *   rows, cols  host arrays of n_mats dimensions (> 0);
+ *   world       number of ranks (> 0);
+ *   owner       host array of n_mats entries, written with ranks 0..world-1.
+ * The result depends only on the arguments: every rank computes the same
+ * assignment without communicating.  Host only: touches no GPU.  Returns
+ * MUON_OK (also for n_mats == 0) or MUON_ERR_INVALID_ARG (n_mats < 0,
+ * world <= 0, a null array, a dimension <= 0), in which case owner is not
+ * written. */
+muon_status_t muon_partition(const int64_t* rows, const int64_t* cols, int n_mats, int world, int* owner);
+
 #ifdef __cplusplus
 }
 #endif

@@ -32,7 +32,8 @@ MUON_F32 = 1
 #: every symbol include/muon.h declares
 EXPORTS = ["muon_workspace_size", "muon_step", "ns5_workspace_size", "ns5", "ns5_bank",
            "ns5_bank_workspace_size", "muon_device_status", "muon_status_str",
-           "ns5_workspace_layout", "muon_set_debug", "muon_kernel_times", "ns5_noalloc"]
+           "ns5_workspace_layout", "muon_set_debug", "muon_kernel_times", "ns5_noalloc",
+           "muon_partition"]
 
 #: bytes of the static device scratch ns5_noalloc uses (MUON_NOALLOC_SCRATCH_BYTES)
 NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -98,6 +99,8 @@ def lib():
     L.muon_kernel_times.restype = c_int
     L.ns5_noalloc.argtypes = [c_vp, c_int, c_vp, c_int, c_i64, c_i64, c_int, c_vp]
     L.ns5_noalloc.restype = c_int
+    L.muon_partition.argtypes = [P(c_i64), P(c_i64), c_int, c_int, P(c_int)]
+    L.muon_partition.restype = c_int
     _lib = L
     return L
 
@@ -268,3 +271,15 @@ def ns5_noalloc(G, ns_steps=5, out=None, stream=None):
                            _stream(stream))
     _check(st, "ns5_noalloc")
     return out[0] if squeeze else out
+
+
+def partition(shapes, world):
+    """Owner rank of each matrix of a bank of (rows, cols) shapes when the
+    step runs on `world` processes: heaviest Newton-Schulz work first, each
+    matrix to the least-loaded rank (muon_partition; host only)."""
+    n = len(shapes)
+    rows = (ctypes.c_int64 * max(n, 1))(*[int(r) for r, _ in shapes])
+    cols = (ctypes.c_int64 * max(n, 1))(*[int(c) for _, c in shapes])
+    owner = (ctypes.c_int * max(n, 1))()
+    _check(lib().muon_partition(rows, cols, n, int(world), owner), "muon_partition")
+    return [owner[i] for i in range(n)]
