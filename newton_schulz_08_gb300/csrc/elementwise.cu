@@ -25,6 +25,7 @@ namespace muon {
 namespace {
 
 constexpr int kEwThreads = 256;
+constexpr int kNormBatch = 4;  // normalise: 8-element vectors per thread in flight
 
 // Programmatic dependent launch: wait for the previous grid's results, then
 // let the next grid be scheduled.
@@ -81,10 +82,10 @@ __device__ __forceinline__ float momentum_u(float g, float* buf, long long i, fl
 
 }  // namespace
 
-__global__ void __launch_bounds__(kEwThreads) momentum_cast_kernel(const __grid_constant__ K1Params P) {
+__global__ void __launch_bounds__(kEwThreads, 4) momentum_cast_kernel(const __grid_constant__ K1Params P) {
   ptx_grid_dep_wait();
   __shared__ float red[kEwThreads / 32];
-  __shared__ float tile[64][65];
+  __shared__ float tile[2][64][65];
   // which matrix: largest i with block_begin[i] <= blockIdx.x
   int lo = 0, hi = P.n - 1;
   while (lo < hi) {
@@ -194,90 +195,131 @@ __global__ void __launch_bounds__(kEwThreads) momentum_cast_kernel(const __grid_
       }
     }
   } else {
-    // tall: X = u^T (C x R).  64 rows of u per block, 64 x 64 tiles through
-    // shared memory so that both the reads of u and the writes of X are
-    // contiguous across a warp.  Reads: a thread takes 4 consecutive
-    // columns of 4 rows (float4 buf, 8-byte bf16 g); writes: a thread stores
-    // 16 consecutive entries of one X row (two 16-byte stores).
-    const int r0 = b * 64;
+    // tall: X = u^T (C x R).  A block covers 64 rows x kTallCols columns of
+    // u, in 64 x 64 tiles through a double-buffered shared tile, so that both
+    // the reads of u and the writes of X are contiguous across a warp.  A
+    // thread loads 4 consecutive columns of 4 rows (float4 buf, 8-byte bf16
+    // or 16-byte fp32 g) and stores 16 consecutive entries of one X row (two
+    // 16-byte stores); the next tile's loads are issued before the current
+    // tile is written out.
+    const int ncb = (C + kTallCols - 1) / kTallCols;
+    const int r0 = (b / ncb) * 64;
+    const int cb0 = (b % ncb) * kTallCols;
+    const int cb1 = min(C, cb0 + kTallCols);
     const int tid = threadIdx.x;
-    const bool vec_in = (C & 3) == 0;
-    for (int c0 = 0; c0 < C; c0 += 64) {
-      const int cl = (tid & 15) * 4;
+    const int cl = (tid & 15) * 4;  // tile columns cl .. cl + 3
+    const int rq = tid >> 4;        // tile rows rq + 16 k
+    auto write_out = [&](int c0, float (*tl)[65]) {
+      const int cc = tid >> 2;        // X row c0 + cc
+      const int rb = (tid & 3) * 16;  // X columns r0 + rb .. + 15
+      const int c = c0 + cc;
+      if (c < cb1) {
+        __nv_bfloat16* xd = M.x + static_cast<long long>(c) * M.ldx + r0 + rb;
+        if (r0 + rb + 16 <= R) {
+          uint32_t w[8];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int rr = (tid >> 4) + 16 * k;
-        const int r = r0 + rr, c = c0 + cl;
-        float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        if (r < R && vec_in && c + 3 < C) {
-          const long long i = static_cast<long long>(r) * C + c;
-          float g[4];
-          if (M.g_f32) {
-            const float4 v = *reinterpret_cast<const float4*>(static_cast<const float*>(M.g) + i);
-            g[0] = v.x; g[1] = v.y; g[2] = v.z; g[3] = v.w;
-          } else {
-            const uint2 v = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(M.g) + i);
-            g[0] = __uint_as_float(v.x << 16);
-            g[1] = __uint_as_float(v.x & 0xFFFF0000u);
-            g[2] = __uint_as_float(v.y << 16);
-            g[3] = __uint_as_float(v.y & 0xFFFF0000u);
+          for (int j = 0; j < 8; ++j) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(tl[rb + 2 * j][cc], tl[rb + 2 * j + 1][cc]);
+            w[j] = *reinterpret_cast<const uint32_t*>(&h);
           }
-          float u[4];
-          if (M.buf) {
-            float4* bp = reinterpret_cast<float4*>(M.buf + i);
-            float4 bv = *bp;
-            bv.x = fmaf(P.mu, bv.x, g[0]);
-            bv.y = fmaf(P.mu, bv.y, g[1]);
-            bv.z = fmaf(P.mu, bv.z, g[2]);
-            bv.w = fmaf(P.mu, bv.w, g[3]);
-            *bp = bv;
-            u[0] = P.nesterov ? fmaf(P.mu, bv.x, g[0]) : bv.x;
-            u[1] = P.nesterov ? fmaf(P.mu, bv.y, g[1]) : bv.y;
-            u[2] = P.nesterov ? fmaf(P.mu, bv.z, g[2]) : bv.z;
-            u[3] = P.nesterov ? fmaf(P.mu, bv.w, g[3]) : bv.w;
-          } else {
-            u[0] = g[0]; u[1] = g[1]; u[2] = g[2]; u[3] = g[3];
-          }
+          reinterpret_cast<uint4*>(xd)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          reinterpret_cast<uint4*>(xd)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        } else {
+          for (int j = 0; j < 16 && r0 + rb + j < R; ++j) xd[j] = __float2bfloat16_rn(tl[rb + j][cc]);
+        }
+      }
+    };
+    if ((C & 3) == 0) {
+      // g and buf of one tile in registers (g raw: fp32 x 4, or bf16 x 4 in
+      // the first two words)
+      float4 gq[4], bq[4];
+      auto load_tile = [&](int c0) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            x[j] = bf16_round(u[j]);
-            ss = fmaf(x[j], x[j], ss);
+        for (int k = 0; k < 4; ++k) {
+          const int r = r0 + rq + 16 * k, c = c0 + cl;
+          if (r < R && c < cb1) {
+            const long long i = static_cast<long long>(r) * C + c;
+            if (M.g_f32) {
+              gq[k] = *reinterpret_cast<const float4*>(static_cast<const float*>(M.g) + i);
+            } else {
+              const uint2 v = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(M.g) + i);
+              gq[k].x = __uint_as_float(v.x);
+              gq[k].y = __uint_as_float(v.y);
+            }
+            if (M.buf) bq[k] = *reinterpret_cast<const float4*>(M.buf + i);
           }
-        } else if (r < R) {
-          for (int j = 0; j < 4; ++j) {
-            if (c + j < C) {
-              const long long i = static_cast<long long>(r) * C + c + j;
-              const float u = momentum_u(load_g(M.g, M.g_f32, i), M.buf, i, P.mu, P.nesterov);
-              x[j] = bf16_round(u);
+        }
+      };
+      load_tile(cb0);
+      int tb = 0;
+      for (int c0 = cb0; c0 < cb1; c0 += 64, tb ^= 1) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int rr = rq + 16 * k;
+          const int r = r0 + rr, c = c0 + cl;
+          float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          if (r < R && c < cb1) {
+            float g[4];
+            if (M.g_f32) {
+              g[0] = gq[k].x; g[1] = gq[k].y; g[2] = gq[k].z; g[3] = gq[k].w;
+            } else {
+              const uint32_t w0 = __float_as_uint(gq[k].x), w1 = __float_as_uint(gq[k].y);
+              g[0] = __uint_as_float(w0 << 16);
+              g[1] = __uint_as_float(w0 & 0xFFFF0000u);
+              g[2] = __uint_as_float(w1 << 16);
+              g[3] = __uint_as_float(w1 & 0xFFFF0000u);
+            }
+            float u[4];
+            if (M.buf) {
+              float4 bv = bq[k];
+              bv.x = fmaf(P.mu, bv.x, g[0]);
+              bv.y = fmaf(P.mu, bv.y, g[1]);
+              bv.z = fmaf(P.mu, bv.z, g[2]);
+              bv.w = fmaf(P.mu, bv.w, g[3]);
+              *reinterpret_cast<float4*>(M.buf + static_cast<long long>(r) * C + c) = bv;
+              u[0] = P.nesterov ? fmaf(P.mu, bv.x, g[0]) : bv.x;
+              u[1] = P.nesterov ? fmaf(P.mu, bv.y, g[1]) : bv.y;
+              u[2] = P.nesterov ? fmaf(P.mu, bv.z, g[2]) : bv.z;
+              u[3] = P.nesterov ? fmaf(P.mu, bv.w, g[3]) : bv.w;
+            } else {
+              u[0] = g[0]; u[1] = g[1]; u[2] = g[2]; u[3] = g[3];
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              x[j] = bf16_round(u[j]);
               ss = fmaf(x[j], x[j], ss);
             }
           }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) tile[tb][rr][cl + j] = x[j];
         }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) tile[rr][cl + j] = x[j];
+        // one barrier per tile: the other buffer was last read before the
+        // previous tile's barrier
+        __syncthreads();
+        if (c0 + 64 < cb1) load_tile(c0 + 64);
+        write_out(c0, tile[tb]);
       }
-      __syncthreads();
-      {
-        const int cc = tid >> 2;          // X row c0 + cc
-        const int rb = (tid & 3) * 16;    // X columns r0 + rb .. + 15
-        const int c = c0 + cc;
-        if (c < C) {
-          __nv_bfloat16* xd = M.x + static_cast<long long>(c) * M.ldx + r0 + rb;
-          if (r0 + rb + 16 <= R) {
-            uint32_t w[8];
+    } else {
+      for (int c0 = cb0; c0 < cb1; c0 += 64) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const __nv_bfloat162 h = __floats2bfloat162_rn(tile[rb + 2 * j][cc], tile[rb + 2 * j + 1][cc]);
-              w[j] = *reinterpret_cast<const uint32_t*>(&h);
+        for (int k = 0; k < 4; ++k) {
+          const int rr = rq + 16 * k;
+          const int r = r0 + rr;
+          for (int j = 0; j < 4; ++j) {
+            const int c = c0 + cl + j;
+            float x = 0.0f;
+            if (r < R && c < cb1) {
+              const long long i = static_cast<long long>(r) * C + c;
+              x = bf16_round(momentum_u(load_g(M.g, M.g_f32, i), M.buf, i, P.mu, P.nesterov));
+              ss = fmaf(x, x, ss);
             }
-            reinterpret_cast<uint4*>(xd)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            reinterpret_cast<uint4*>(xd)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          } else {
-            for (int j = 0; j < 16 && r0 + rb + j < R; ++j) xd[j] = __float2bfloat16_rn(tile[rb + j][cc]);
+            tile[0][rr][cl + j] = x;
           }
         }
+        __syncthreads();
+        write_out(c0, tile[0]);
+        __syncthreads();
       }
-      __syncthreads();
     }
   }
 
@@ -285,7 +327,7 @@ __global__ void __launch_bounds__(kEwThreads) momentum_cast_kernel(const __grid_
   if (threadIdx.x == 0) P.partials[M.part_off + b] = s;
 }
 
-__global__ void __launch_bounds__(kEwThreads) normalise_kernel(const __grid_constant__ NormParams P) {
+__global__ void __launch_bounds__(kEwThreads, 5) normalise_kernel(const __grid_constant__ NormParams P) {
   ptx_grid_dep_wait();
   __shared__ float red[kEwThreads / 32];
   __shared__ float sh_d;
@@ -296,6 +338,33 @@ __global__ void __launch_bounds__(kEwThreads) normalise_kernel(const __grid_cons
   const int idx = local / K.blocks_per_mat;
   const int b = local - idx * K.blocks_per_mat;
   const MatInfo mi = P.table[K.mat_begin + idx];
+
+  __nv_bfloat16* X = K.x + static_cast<long long>(idx) * K.m * K.ldx;
+  const int r0 = b * K.rows_per_block;
+  const int r1 = min(K.m, r0 + K.rows_per_block);
+  const int n = K.n;
+  const bool vec = (n & 7) == 0;
+  const int cv = n >> 3;  // 8-element vectors per row
+  const long long nvec = vec ? static_cast<long long>(r1 - r0) * cv : 0;
+  // a batch: kNormBatch vectors of 8 per thread, all loads issued before any
+  // store; the first batch is loaded before the norm is known, so that the
+  // reduction of the partials below overlaps its latency
+  uint4 w[kNormBatch];
+  uint4* ptr[kNormBatch];
+  bool have[kNormBatch];
+  auto load_batch = [&](long long v0) {
+#pragma unroll
+    for (int h = 0; h < kNormBatch; ++h) {
+      const long long v = v0 + h * kEwThreads;
+      have[h] = v < nvec;
+      const long long vv = have[h] ? v : 0;
+      const int r = r0 + static_cast<int>(vv / cv);
+      const int cc = static_cast<int>(vv % cv) * 8;
+      ptr[h] = reinterpret_cast<uint4*>(X + static_cast<long long>(r) * K.ldx + cc);
+      if (have[h]) w[h] = *ptr[h];
+    }
+  };
+  if (vec) load_batch(threadIdx.x);
 
   // the matrix's norm: fixed-order sum of its partials
   float part = 0.0f;
@@ -309,29 +378,11 @@ __global__ void __launch_bounds__(kEwThreads) normalise_kernel(const __grid_cons
   __syncthreads();
   const float d = sh_d;
 
-  __nv_bfloat16* X = K.x + static_cast<long long>(idx) * K.m * K.ldx;
-  const int r0 = b * K.rows_per_block;
-  const int r1 = min(K.m, r0 + K.rows_per_block);
-  const int n = K.n;
-  if ((n & 7) == 0) {
-    const int cv = n >> 3;
-    const long long nvec = static_cast<long long>(r1 - r0) * cv;
-    for (long long v0 = threadIdx.x; v0 < nvec; v0 += 2 * kEwThreads) {
-      uint4* ptr[2];
-      uint4 w[2];
-      bool have[2];
+  if (vec) {
+    for (long long v0 = threadIdx.x; v0 < nvec; v0 += kNormBatch * kEwThreads) {
+      if (v0 != threadIdx.x) load_batch(v0);
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const long long v = v0 + h * kEwThreads;
-        have[h] = v < nvec;
-        const long long vv = have[h] ? v : v0;
-        const int r = r0 + static_cast<int>(vv / cv);
-        const int cc = static_cast<int>(vv % cv) * 8;
-        ptr[h] = reinterpret_cast<uint4*>(X + static_cast<long long>(r) * K.ldx + cc);
-        if (have[h]) w[h] = *ptr[h];
-      }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < kNormBatch; ++h) {
         if (!have[h]) continue;
         uint32_t ws[4] = {w[h].x, w[h].y, w[h].z, w[h].w};
 #pragma unroll

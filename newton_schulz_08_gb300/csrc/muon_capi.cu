@@ -142,7 +142,7 @@ bool build_plan(const std::vector<JobMat>& mats, Plan& P) {
     int rpb, blocks;
     if (M.R > M.C) {
       rpb = 64;
-      blocks = static_cast<int>(ceil_div(M.R, 64));
+      blocks = static_cast<int>(ceil_div(M.R, 64) * ceil_div(M.C, kTallCols));
     } else {
       rpb = static_cast<int>(std::max<long long>(1, kElemsPerBlock / M.C));
       blocks = static_cast<int>(ceil_div(M.R, rpb));

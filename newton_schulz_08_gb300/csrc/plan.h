@@ -16,6 +16,7 @@ namespace muon {
 
 constexpr int kMaxClasses = 8;     // shape classes per launch
 constexpr int kK1MaxMats = 96;     // matrices per momentum-pass launch
+constexpr int kTallCols = 256;  // momentum pass: a tall matrix's block is 64 rows x 256 columns
 
 // device status word bits (kept in the workspace header)
 constexpr int kStatusNonFinite = 1;
