@@ -17,11 +17,18 @@ Source of the method:
 Three steps are not printed on that page; the readings taken here are stated in
 ``oracle.muon`` next to the code that takes them.
 
+``oracle.adam`` restates the Adam step with cautious weight decay that the page
+on the modded-nanogpt record "2026-06-11_RecursiveFromBest" (lqnn.cn,
+news/184262, section "3.3 bigram 与 value-embedding 银行上的 C-Optim / 谨慎
+Adam") describes for the embedding-type banks; its readings are stated there.
+
 Pin status: every public function is pinned by the CPU tests
 (closed form via SVD, invariants, brute force in exact rational arithmetic,
-bit-exact bf16 rounding against an independent routine).
+bit-exact bf16 rounding against an independent routine; for Adam: closed
+forms, torch.optim.Adam / AdamW special cases, hand-worked mask values).
 """
 
+from .adam import ADAM_DEFAULTS, adam_constants, adam_step, cautious_mask
 from .bf16 import round_to_bf16, BF16_MAX
 from .muon import (
     NS_COEFFS,
@@ -40,6 +47,10 @@ from .muon import (
 )
 
 __all__ = [
+    "ADAM_DEFAULTS",
+    "adam_constants",
+    "adam_step",
+    "cautious_mask",
     "round_to_bf16",
     "BF16_MAX",
     "NS_COEFFS",
