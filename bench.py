@@ -48,6 +48,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # ------------------------------------------------------------------ workloads
 def workload_shapes(name):
     from newton_schulz_08_gb300 import inputs
+    if name == "adam":
+        return inputs.adam_bank_shapes()
     return {
         "gpt2": inputs.gpt2_shapes(),
         "gpt1p5b": inputs.gpt1p5b_shapes(),
@@ -58,6 +60,8 @@ def workload_shapes(name):
 
 
 NS5_ONLY = {"spectra"}
+ADAM_WORKLOADS = {"adam"}
+ADAM_HP = {"lr": 3e-3, "beta1": 0.9, "beta2": 0.95, "eps": 1e-10, "weight_decay": 0.05, "cautious": True}
 
 
 WORKLOAD_DESC = {
@@ -69,6 +73,8 @@ WORKLOAD_DESC = {
     "single": "single 128x512 matrix, fp32 grad",
     "spectra": "spectra sweep, Newton-Schulz only (ns5_bank): 64 x 1024x1024 and 16 x 4096x4096 bf16 "
                "G = U diag(s) V^T, s log-uniform in [1e-4, 1]",
+    "adam": "Adam step with cautious weight decay on an embedding-type bank: 4 tables of 50304x768, "
+            "154.53M fp32 params, bf16 grads, fp32 moments, step 10 of training",
 }
 
 
@@ -192,11 +198,54 @@ def oracle_sample(shapes, budget_s, min_mats=1, mode="bf16"):
     return done, t_total
 
 
+def adam_oracle_sample(shapes, budget_s, min_tensors=1):
+    """Time the oracle's float32 Adam step on whole tensors of the bank taken
+    in order (wrapping around) until `budget_s` seconds have passed; returns
+    (parameters done, seconds)."""
+    import oracle
+    from newton_schulz_08_gb300 import inputs
+    done, n_params, t_total, i = 0, 0, 0.0, 0
+    hp = dict(ADAM_HP)
+    while done < min_tensors or t_total < budget_s:
+        shape = shapes[i % len(shapes)]
+        p, m, v, g = inputs.adam_state(shape, i)
+        g = oracle.round_to_bf16(g)
+        t0 = time.perf_counter()
+        oracle.adam_step(p, g, m, v, inputs.ADAM_STEP, lr=hp["lr"], beta1=hp["beta1"], beta2=hp["beta2"],
+                         eps=hp["eps"], wd=hp["weight_decay"], cautious=hp["cautious"], mode="fp32")
+        t_total += time.perf_counter() - t0
+        done += 1
+        n_params += int(np.prod(shape))
+        i += 1
+    return n_params, t_total
+
+
 def run_reference(args, rank, world):
     """Reference arm: the CPU oracle, as it stands, on the host cores."""
     if rank != 0:
         return
     shapes = workload_shapes(args.workload)
+    if args.workload in ADAM_WORKLOADS:
+        for _ in range(args.warmup):
+            adam_oracle_sample(shapes, 0.0)
+        total, total_t = 0, 0.0
+        for _ in range(args.steps):
+            n, t = adam_oracle_sample(shapes, 0.0)
+            total += n
+            total_t += t
+        value = total / total_t
+        line = {
+            "impl": "reference", "metric": "adam_step_params_per_s", "value": value, "unit": "params/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * total_t / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC[args.workload]},
+            "cpu_baseline": {"value": value, "unit": "params/s", "cores": cpu_threads(), "kind": "oracle",
+                             "sample": "one 50304x768 table of the bank per step (float32 oracle)"},
+            "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(line), flush=True)
+        return
     # size each step so the whole run stays within about two minutes
     n0, t0 = oracle_sample(shapes, 0.0, min_mats=1)
     per_mat = t0 / n0
@@ -308,6 +357,10 @@ def main():
     device = torch.device("cuda", local)
     if world > 1:
         dist.init_process_group("nccl", device_id=device)
+
+    if args.workload in ADAM_WORKLOADS:
+        run_adam(args, rank, world, device)
+        return
 
     L = muon.lib()
     ids, shapes = rank_bank(workload_shapes(args.workload), world, rank)
@@ -490,6 +543,111 @@ def main():
                                 "kind": "oracle",
                                 "sample": f"{n_cpu} matrices of the bank in order, full Muon step, "
                                           f"bf16-emulating oracle, {t_cpu:.1f} s"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_adam(args, rank, world, device):
+    """The Adam step with cautious weight decay on the embedding-type bank:
+    one adam_step call (one kernel launch) per step."""
+    import torch
+    import torch.distributed as dist
+
+    from newton_schulz_08_gb300 import inputs, muon
+
+    ids, shapes = rank_bank(workload_shapes(args.workload), world, rank)
+    n_total = sum(int(np.prod(s)) for s in workload_shapes(args.workload)) * world
+    n_local = sum(int(np.prod(s)) for s in shapes)
+    P, M, V, G = [], [], [], []
+    for i, shp in zip(ids, shapes):
+        p, m, v, g = inputs.adam_state(shp, i)
+        P.append(torch.from_numpy(p).to(device))
+        M.append(torch.from_numpy(m).to(device))
+        V.append(torch.from_numpy(v).to(device))
+        G.append(torch.from_numpy(g).to(device).to(torch.bfloat16))
+    hp = dict(ADAM_HP)
+    stream = torch.cuda.current_stream(device)
+
+    def step(k):
+        muon.adam_step(P, G, M, V, inputs.ADAM_STEP + k, lr=hp["lr"], beta1=hp["beta1"], beta2=hp["beta2"],
+                       eps=hp["eps"], weight_decay=hp["weight_decay"], cautious=hp["cautious"], stream=stream)
+
+    def barrier():
+        torch.cuda.synchronize(device)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(device)
+
+    launches_per_step = (len(shapes) + 63) // 64
+    for k in range(args.warmup):
+        step(k)
+    barrier()
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for k in range(args.steps):
+        step(args.warmup + k)
+    e1.record(stream)
+    barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, device)
+
+    # e2e: this step's gradients in from pinned host memory, parameters out
+    g_host = [g.cpu().pin_memory() for g in G]
+    p_host = [torch.empty(p.shape, dtype=p.dtype).pin_memory() for p in P]
+    e_steps = max(3, args.steps // 4)
+    barrier()
+    e0.record(stream)
+    for k in range(e_steps):
+        for gd, gh in zip(G, g_host):
+            gd.copy_(gh, non_blocking=True)
+        step(args.warmup + args.steps + k)
+        for pd, ph in zip(P, p_host):
+            ph.copy_(pd, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, world, device)
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    bytes_per_step = 26.0 * n_local  # p, m, v read + written (fp32), g read (bf16)
+    achieved = bytes_per_step / (ms * 1e-3) / 1e9
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tfile):
+        with open(tfile) as f:
+            traffic = json.load(f).get(args.workload, {}).get("adam")
+    line = {
+        "metric": "adam_step_params_per_s", "value": n_total / (ms * 1e-3), "unit": "params/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC[args.workload], "tensors": len(shapes) * world,
+                   "params": n_total, "hyper_parameters": hp,
+                   "l2": "no flush: the bank's 2.2 GB of state exceeds the 129 MB L2",
+                   "parallelism": (f"{world} ranks, each owning a share of {world} banks (no data exchanged)"
+                                   if world > 1 else "1 GPU")},
+        "roofline": {"kernel": "adam", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "peak_source": f"{peak_src} (hbm_gbs)"},
+        "e2e": {"value": n_total / (e2e_ms * 1e-3), "unit": "params/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": int(sum(g.numel() * g.element_size() for g in G)),
+                "d2h_bytes_per_step": int(sum(p.numel() * p.element_size() for p in P))},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        n_cpu, t_cpu = adam_oracle_sample(shapes, args.cpu_budget)
+        line["cpu_baseline"] = {"value": n_cpu / t_cpu, "unit": "params/s", "cores": cpu_threads(),
+                                "kind": "oracle",
+                                "sample": f"{n_cpu} params (whole tables in bank order), float32 oracle, "
+                                          f"{t_cpu:.1f} s"}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -191,6 +191,47 @@ int muon_kernel_times(double* ms, int* launches, int n_kinds);
 muon_status_t ns5_noalloc(const void* G, int g_dtype, void* O, int batch, int64_t rows,
                           int64_t cols, int ns_steps, void* stream);
 
+/* One tensor of an Adam step: caller-owned DEVICE memory, contiguous. */
+typedef struct adam_tensor_desc {
+  float* param;        /* numel fp32 values, updated in place */
+  const void* grad;    /* numel values of grad_dtype, read only */
+  float* exp_avg;      /* first moment m, numel fp32, updated in place */
+  float* exp_avg_sq;   /* second moment v, numel fp32, updated in place */
+  int64_t numel;       /* > 0 */
+  int32_t grad_dtype;  /* MUON_BF16 or MUON_F32 */
+  int32_t reserved;
+} adam_tensor_desc;
+
+/* Adam step with cautious weight decay over a list of tensors: the
+ * optimizer of the embedding-type parameters (bigram table, value
+ * embeddings) that the page on the modded-nanogpt record
+ * "2026-06-11_RecursiveFromBest" (lqnn.cn, news/184262), section "3.3 bigram
+ * 与 value-embedding 银行上的 C-Optim / 谨慎 Adam", pairs with Muon: decay is
+ * applied only where the update and the parameter agree in sign.  Adam is
+ * the textbook algorithm.  Per element, t = step, bc1 = 1 - beta1^t,
+ * bc2 = 1 - beta2^t:
+ *   m <- beta1 m + (1 - beta1) g;   v <- beta2 v + (1 - beta2) g^2
+ *   u  = (m / bc1) / (sqrt(v / bc2) + eps)
+ *   p <- p - lr (u + weight_decay * p * mask)
+ * with mask = (u > 0 and p > 0) or (u < 0 and p < 0) when `cautious` is
+ * non-zero, mask = 1 otherwise (plain decoupled decay).  Arithmetic: float32,
+ * each operation one IEEE-rounded operation in the order above, no fused
+ * multiply-add; (1 - beta), bc1 and bc2 are formed in double from the float
+ * arguments and rounded once to float.  Updates are independent per element,
+ * so the result does not depend on the launch configuration.
+ *   tensors, n_tensors  host array of descriptors (n_tensors = 0: no-op);
+ *   step                1 for the first step (>= 1);
+ *   beta1, beta2 in [0, 1); eps >= 0; lr, weight_decay finite.
+ * Errors (nothing enqueued): MUON_ERR_INVALID_ARG (null pointer, numel <= 0,
+ * bad dtype, step < 1, hyper-parameter out of range, beta^step rounding to
+ * 1), MUON_ERR_MISALIGNED (a pointer not 16-byte aligned),
+ * MUON_ERR_ALIASING (a written array overlaps another written array or a
+ * gradient), MUON_ERR_TOO_LARGE, MUON_ERR_CUDA (launch failure).  Non-finite
+ * values propagate.  Asynchronous on `stream` (a cudaStream_t); one launch
+ * per 64 tensors; needs no workspace. */
+muon_status_t adam_step(const adam_tensor_desc* tensors, int n_tensors, float lr, float beta1, float beta2,
+                        float eps, float weight_decay, int step, int cautious, void* stream);
+
 /* Assigns each matrix of a bank to one of `world` ranks, for running the
  * step on several GPUs, one process per GPU, each updating only the matrices
  * it owns (every matrix's step depends on that matrix alone, so no data is

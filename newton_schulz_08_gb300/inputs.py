@@ -27,6 +27,13 @@ Workloads (matrix shapes are rows x cols as stored, row-major):
 * ``gpt1p5b``  1.5B-shaped bank, d = 1600, 48 layers of 4 x (1600x1600),
                6400x1600, 1600x6400 (288 matrices, 1.4746 B parameters);
                as ``gpt2`` otherwise, one step.
+* ``adam``     embedding-type bank for the Adam step: 4 tables of
+               50304 x 768 (GPT-2-124M's padded vocabulary x width; the page
+               names the bigram and value-embedding banks but not their
+               sizes), 154.53 M fp32 parameters; p ~ N(0, 0.02^2), first
+               moment ~ N(0, 1e-3^2), second moment = (N(0, 1e-3^2))^2
+               (non-negative), grads ~ N(0, 1e-3^2) bf16; the state is that
+               of a step in mid-training (step count 10).
 """
 
 import numpy as np
@@ -39,6 +46,7 @@ SEED_U = 4_000_000
 SEED_V = 5_000_000
 SEED_S = 6_000_000
 SEED_RECT = 7_000_000
+SEED_ADAM = 8_000_000  # + 4 * tensor + {0: p, 1: m, 2: v, 3: g} + 1_000 * step
 
 
 def gpt2_shapes(d=768, layers=12):
@@ -84,6 +92,25 @@ def buffer(shape, i, std=1e-3):
 def grad(shape, i, step=0, std=1e-3):
     """float32 draw; bf16 banks round it to bfloat16 when uploading."""
     return normal(shape, std, SEED_G + 10_000 * step + i)
+
+
+ADAM_TABLE = (50304, 768)
+ADAM_STEP = 10
+
+
+def adam_bank_shapes(tables=4):
+    return [ADAM_TABLE] * tables
+
+
+def adam_state(shape, i, step=0):
+    """Tensor i of an Adam bank: (p, m, v, g) float32 (g is rounded to
+    bfloat16 when a bank uploads bf16 gradients).  Gradients differ per step."""
+    rng = [np.random.default_rng(SEED_ADAM + 4 * i + k) for k in range(3)]
+    p = rng[0].standard_normal(shape, dtype=np.float32) * np.float32(0.02)
+    m = rng[1].standard_normal(shape, dtype=np.float32) * np.float32(1e-3)
+    v = np.square(rng[2].standard_normal(shape, dtype=np.float32) * np.float32(1e-3))
+    g = np.random.default_rng(SEED_ADAM + 4 * i + 3 + 1_000 * step).standard_normal(shape, dtype=np.float32)
+    return p, m, v, g * np.float32(1e-3)
 
 
 def haar(n, seed):

@@ -33,7 +33,7 @@ MUON_F32 = 1
 EXPORTS = ["muon_workspace_size", "muon_step", "ns5_workspace_size", "ns5", "ns5_bank",
            "ns5_bank_workspace_size", "muon_device_status", "muon_status_str",
            "ns5_workspace_layout", "muon_set_debug", "muon_kernel_times", "ns5_noalloc",
-           "muon_partition"]
+           "muon_partition", "adam_step"]
 
 #: bytes of the static device scratch ns5_noalloc uses (MUON_NOALLOC_SCRATCH_BYTES)
 NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -58,6 +58,12 @@ class muon_ws_layout(ctypes.Structure):
     _fields_ = [("x_offset", ctypes.c_size_t * 2), ("a_offset", ctypes.c_size_t),
                 ("b_offset", ctypes.c_size_t), ("ldx", ctypes.c_int64), ("lda", ctypes.c_int64),
                 ("m", ctypes.c_int64), ("n", ctypes.c_int64)]
+
+
+class adam_tensor_desc(ctypes.Structure):
+    _fields_ = [("param", ctypes.c_void_p), ("grad", ctypes.c_void_p), ("exp_avg", ctypes.c_void_p),
+                ("exp_avg_sq", ctypes.c_void_p), ("numel", ctypes.c_int64),
+                ("grad_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 _lib = None
@@ -101,6 +107,8 @@ def lib():
     L.ns5_noalloc.restype = c_int
     L.muon_partition.argtypes = [P(c_i64), P(c_i64), c_int, c_int, P(c_int)]
     L.muon_partition.restype = c_int
+    L.adam_step.argtypes = [P(adam_tensor_desc), c_int, c_f, c_f, c_f, c_f, c_f, c_int, c_int, c_vp]
+    L.adam_step.restype = c_int
     _lib = L
     return L
 
@@ -283,3 +291,25 @@ def partition(shapes, world):
     owner = (ctypes.c_int * max(n, 1))()
     _check(lib().muon_partition(rows, cols, n, int(world), owner), "muon_partition")
     return [owner[i] for i in range(n)]
+
+
+def adam_step(params, grads, exp_avgs, exp_avg_sqs, step, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8,
+              weight_decay=0.0, cautious=True, stream=None):
+    """Adam step with cautious weight decay over lists of CUDA tensors, in
+    place (fp32 params and moments; bf16 or fp32 grads).  See adam_step in
+    include/muon.h for the arithmetic."""
+    n = len(params)
+    if not (len(grads) == len(exp_avgs) == len(exp_avg_sqs) == n):
+        raise ValueError("params, grads, exp_avgs, exp_avg_sqs must have the same length")
+    arr = (adam_tensor_desc * max(n, 1))()
+    for i, (p, g, m, v) in enumerate(zip(params, grads, exp_avgs, exp_avg_sqs)):
+        for t in (p, m, v):
+            if t.dtype != torch.float32 or not t.is_contiguous() or not t.is_cuda:
+                raise ValueError("params and moments must be contiguous float32 CUDA tensors")
+        if not (p.numel() == g.numel() == m.numel() == v.numel()) or not g.is_contiguous():
+            raise ValueError("tensor sizes differ or a gradient is not contiguous")
+        arr[i] = adam_tensor_desc(p.data_ptr(), g.data_ptr(), m.data_ptr(), v.data_ptr(), p.numel(),
+                                  _dtype_code(g), 0)
+    st = lib().adam_step(arr, n, float(lr), float(beta1), float(beta2), float(eps), float(weight_decay),
+                         int(step), int(bool(cautious)), _stream(stream))
+    _check(st, "adam_step")

@@ -34,9 +34,10 @@ Per element, with bc1 = 1 - beta1^t and bc2 = 1 - beta2^t:
 Modes:
   "fp64": every operation in float64 (the definition).
   "fp32": every operation one IEEE float32 operation in the order written
-          above (no fused multiply-add), with the constants (1 - beta1),
-          (1 - beta2), bc1 and bc2 formed in float64 and rounded once to
-          float32 -- the arithmetic the GPU kernel performs.
+          above (no fused multiply-add); the hyper-parameters are rounded to
+          float32 first, and the constants (1 - beta1), (1 - beta2), bc1 and
+          bc2 are formed in float64 from the rounded betas and rounded once
+          to float32 -- the arithmetic the GPU kernel performs.
 """
 
 import numpy as np
@@ -67,6 +68,8 @@ def adam_step(p, g, m, v, step, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.
         f = np.float32
     else:
         raise ValueError(mode)
+    if mode == "fp32":
+        beta1, beta2 = float(np.float32(beta1)), float(np.float32(beta2))
     omb1, omb2, bc1, bc2 = (f(c) for c in adam_constants(beta1, beta2, step))
     b1, b2, lr_, eps_, wd_ = f(beta1), f(beta2), f(lr), f(eps), f(wd)
     p = np.asarray(p, dtype=f)
