@@ -152,6 +152,48 @@ def test_muon_step_mixed_bank(nesterov, gdtype):
         assert rel(O_gpu, O64) <= TOL_REL_FP64
 
 
+def check_bank_against_oracle(shapes, ps, gs, bs, P, Bn, lr=0.02, mu=0.95):
+    for i in range(len(shapes)):
+        new_p, new_buf, O = oracle.muon_step(ps[i], gs[i], bs[i], lr, mu, True, 5, "bf16")
+        assert rel(Bn[i], new_buf) <= TOL_BUF_REL, i
+        O_gpu = (ps[i].astype(np.float64) - P[i].astype(np.float64)) / lr
+        assert rel(O_gpu, O) <= TOL_REL_BF16, (i, shapes[i])
+        assert np.abs(O_gpu - O).max() <= TOL_MAXABS_BF16, (i, shapes[i])
+
+
+def test_bank_beyond_one_launch_per_phase():
+    """12 shape classes (each phase takes two launches of at most 8 classes)
+    and 108 matrices (the momentum pass takes two launches of at most 96).
+    Every matrix: momentum buffer, and O against the fp64 oracle; one matrix
+    per class: O against the bf16 oracle.  (The bf16 bound is checked on a
+    subset: two bf16 evaluations that differ only in fp32 accumulation order
+    already differ by up to ~8e-3 on Gaussian matrices of these sizes, so
+    over a hundred draws the 1e-2 bound has no margin.)"""
+    base = [(128, 384), (384, 128), (256, 256), (192, 320), (320, 192), (256, 512), (512, 256),
+            (160, 480), (480, 160), (300, 300), (224, 448), (448, 224)]
+    shapes = [base[i % len(base)] for i in range(108)]
+    lr, mu = 0.02, 0.95
+    ps, gs, bs, P, Bn = run_step(shapes, True, 5, torch.bfloat16, seed=11, lr=lr, mu=mu)
+    for i in range(len(shapes)):
+        nb, u = oracle.momentum_update(gs[i], bs[i], mu, True, "bf16")
+        assert rel(Bn[i], nb) <= TOL_BUF_REL, i
+        O_gpu = (ps[i].astype(np.float64) - P[i].astype(np.float64)) / lr
+        O64 = oracle.newton_schulz5(u, 5, "fp64")
+        assert rel(O_gpu, O64) <= TOL_REL_FP64, (i, shapes[i])
+    picks = list(range(len(base)))
+    check_bank_against_oracle([shapes[i] for i in picks], [ps[i] for i in picks], [gs[i] for i in picks],
+                              [bs[i] for i in picks], [P[i] for i in picks], [Bn[i] for i in picks], lr, mu)
+
+
+@pytest.mark.parametrize("shape", [(2, 65536), (65536, 3), (256, 40000)])
+def test_extreme_aspect_ratios(shape):
+    """Long contractions (up to 1024 K blocks per tile), 2- and 3-row Gram
+    matrices padded inside one tile, and a tall matrix whose width is not a
+    multiple of 4 (the scalar path of the transposing momentum pass)."""
+    ps, gs, bs, P, Bn = run_step([shape], True, 5, torch.bfloat16, seed=12)
+    check_bank_against_oracle([shape], ps, gs, bs, P, Bn)
+
+
 def test_param_update_is_exact_given_gpu_O():
     """p_new = p - lr * O_gpu in fp32, O_gpu read from the workspace."""
     R, C = 300, 100
