@@ -14,8 +14,9 @@
 //   tall matrices through a shared-memory tile), and one partial sum of
 //   Xraw^2 per block (warp shuffles, then a fixed-order block reduction: the
 //   result does not depend on scheduling).
-// normalise: X0 = bf16(Xraw / (sqrt(sum of the matrix's partials) + 1e-7)),
-//   in place; the partials are summed in a fixed order by every block.
+// normalise: X0 = bf16(Xraw * (1 / (sqrt(sum of the matrix's partials) +
+//   1e-7))), in place; the partials are summed in a fixed order by every
+//   block.
 // apply: after the last step, p <- p - lr * O (or O written), O = X in the
 //   stored orientation.
 #include "plan.h"
@@ -26,6 +27,7 @@ namespace {
 
 constexpr int kEwThreads = 256;
 constexpr int kNormBatch = 4;  // normalise: 8-element vectors per thread in flight
+constexpr int kCastBatch = 8;  // cast-only momentum pass: 8-element vectors per thread in flight
 
 // Programmatic dependent launch: wait for the previous grid's results, then
 // let the next grid be scheduled.
@@ -114,7 +116,40 @@ __global__ void __launch_bounds__(kEwThreads, 4) momentum_cast_kernel(const __gr
     const int r0 = b * M.rows_per_block;
     const int r1 = min(R, r0 + M.rows_per_block);
     const bool vec = (C & 7) == 0;
-    if (vec) {
+    if (vec && !M.buf && !M.g_f32) {
+      // cast only (bf16 G, no momentum buffer): 2 + 2 bytes per element, so
+      // kCastBatch 16-byte vectors per thread are kept in flight
+      const int cv = C >> 3;
+      const long long nvec = static_cast<long long>(r1 - r0) * cv;
+      for (long long v0 = threadIdx.x; v0 < nvec; v0 += kCastBatch * kEwThreads) {
+        uint4 w[kCastBatch];
+        long long iv[kCastBatch];
+#pragma unroll
+        for (int h = 0; h < kCastBatch; ++h) {
+          const long long v = v0 + h * kEwThreads;
+          iv[h] = -1;
+          if (v < nvec) {
+            const int r = r0 + static_cast<int>(v / cv);
+            const int c = static_cast<int>(v % cv) * 8;
+            iv[h] = static_cast<long long>(r) * M.ldx + c;
+            w[h] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(M.g) +
+                                                   static_cast<long long>(r) * C + c);
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < kCastBatch; ++h) {
+          if (iv[h] < 0) continue;
+          const uint32_t ws[4] = {w[h].x, w[h].y, w[h].z, w[h].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float x0 = __uint_as_float(ws[k] << 16), x1 = __uint_as_float(ws[k] & 0xFFFF0000u);
+            ss = fmaf(x0, x0, ss);
+            ss = fmaf(x1, x1, ss);
+          }
+          *reinterpret_cast<uint4*>(M.x + iv[h]) = w[h];
+        }
+      }
+    } else if (vec) {
       const int cv = C >> 3;  // 8-element vectors per row
       const long long nvec = static_cast<long long>(r1 - r0) * cv;
       // two vectors per thread per iteration, all loads issued before any
@@ -377,6 +412,11 @@ __global__ void __launch_bounds__(kEwThreads, 5) normalise_kernel(const __grid_c
   }
   __syncthreads();
   const float d = sh_d;
+  // X0 = bf16(x * r), r = 1/d rounded to float: the product is within 1.5
+  // float ulp of the quotient x/d (an IEEE division: 0.5 ulp) and costs one
+  // instruction instead of a division sequence; after the bf16 rounding the
+  // two differ only for quotients within 2^-8 bf16 ulp of a rounding midpoint
+  const float inv_d = 1.0f / d;
 
   if (vec) {
     for (long long v0 = threadIdx.x; v0 < nvec; v0 += kNormBatch * kEwThreads) {
@@ -387,8 +427,8 @@ __global__ void __launch_bounds__(kEwThreads, 5) normalise_kernel(const __grid_c
         uint32_t ws[4] = {w[h].x, w[h].y, w[h].z, w[h].w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const float lo = __uint_as_float(ws[k] << 16) / d;
-          const float hi = __uint_as_float(ws[k] & 0xFFFF0000u) / d;
+          const float lo = __uint_as_float(ws[k] << 16) * inv_d;
+          const float hi = __uint_as_float(ws[k] & 0xFFFF0000u) * inv_d;
           const __nv_bfloat162 hh = __floats2bfloat162_rn(lo, hi);
           ws[k] = *reinterpret_cast<const uint32_t*>(&hh);
         }
@@ -401,7 +441,7 @@ __global__ void __launch_bounds__(kEwThreads, 5) normalise_kernel(const __grid_c
       const int r = r0 + static_cast<int>(e / n);
       const int cc = static_cast<int>(e % n);
       __nv_bfloat16* p = X + static_cast<long long>(r) * K.ldx + cc;
-      *p = __float2bfloat16_rn(__bfloat162float(*p) / d);
+      *p = __float2bfloat16_rn(__bfloat162float(*p) * inv_d);
     }
   }
 }
