@@ -296,6 +296,63 @@ def max_over_ranks(x, world, device=None):
     return float(t.item())
 
 
+def e2e_pipelined(stream, device, n_steps, in_bufs, in_host, step_fn, out_dev, out_host):
+    """End-to-end timing with host copies: every step uploads its inputs from
+    pinned host memory and reads its result back to pinned host memory.  The
+    copies run on two copy streams and overlap the compute: step k+1's inputs
+    go into the second of two device input buffers while step k runs, and
+    step k's result is snapshotted on the device and read back while step
+    k+1 runs.  in_bufs: two lists of device input tensors; in_host: lists of
+    pinned host tensors (cycled); step_fn(j) runs one step on in_bufs[j];
+    out_dev / out_host: lists of device result tensors and pinned host
+    buffers.  Returns milliseconds per step (CUDA events on `stream`)."""
+    import torch
+    h2d, d2h = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    snap = [torch.empty_like(t) for t in out_dev]
+    ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of buffer j landed
+    ev_used = [torch.cuda.Event() for _ in range(2)]  # the step reading buffer j finished
+    ev_snap, ev_out = torch.cuda.Event(), torch.cuda.Event()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for e in ev_used + [ev_out]:
+        e.record(stream)
+
+    def upload(k, j):
+        h2d.wait_event(ev_used[j])
+        with torch.cuda.stream(h2d):
+            for dst, src in zip(in_bufs[j], in_host[k % len(in_host)]):
+                dst.copy_(src, non_blocking=True)
+        ev_in[j].record(h2d)
+
+    e0.record(stream)
+    upload(0, 0)
+    for k in range(n_steps):
+        j = k % 2
+        if k + 1 < n_steps:
+            upload(k + 1, 1 - j)
+        stream.wait_event(ev_in[j])
+        step_fn(j)
+        ev_used[j].record(stream)
+        stream.wait_event(ev_out)  # the previous snapshot has been read back
+        with torch.cuda.stream(stream):
+            for dst, src in zip(snap, out_dev):
+                dst.copy_(src, non_blocking=True)
+        ev_snap.record(stream)
+        d2h.wait_event(ev_snap)
+        with torch.cuda.stream(d2h):
+            for dst, src in zip(out_host, snap):
+                dst.copy_(src, non_blocking=True)
+        ev_out.record(d2h)
+    stream.wait_event(ev_out)
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / n_steps
+
+
+E2E_NOTE = ("every step uploads its inputs from pinned host memory and reads its result back to pinned host "
+            "memory; the copies run on two copy streams overlapped with compute (next step's inputs into a "
+            "second device buffer; this step's result snapshotted on the device, then read back)")
+
+
 # ------------------------------------------------------------------ GPU arm
 def build_bank(shapes, device, grad_sets, ids=None):
     """Device tensors of the bank: params, bufs, grad sets (flat + views).
@@ -386,9 +443,14 @@ def main():
             if st != 0:
                 raise muon.MuonError(st, "muon_step")
 
-        in_dev, in_host = Gs[0], Gs_host               # e2e: this step's gradients in
-        out_dev = P                                    # e2e: the updated parameters out
-        e2e_arr = descs[0]
+        # e2e: each step's gradients in (device sets 1 and 2 as the two input
+        # buffers), the updated parameters out
+        e2e_in = [[Gs[1]], [Gs[2]]]
+        e2e_host = [[g] for g in Gs_host]
+        e2e_out = [P]
+
+        def e2e_step(j):
+            step(0, descs[1 + j])
         gbytes = 2
     else:
         from newton_schulz_08_gb300 import inputs
@@ -407,15 +469,21 @@ def main():
         cols = (ctypes.c_int64 * n_mats)(*[c for _, c in shapes])
         ws = muon.new_workspace(L.ns5_bank_workspace_size(rows, cols, n_mats), device)
         ws_ptr, ws_bytes = ctypes.c_void_p(ws.data_ptr()), ws.numel()
+        Gflat2 = torch.empty_like(Gflat)
+        gp2 = (ctypes.c_void_p * n_mats)(*[g.data_ptr() for g in views(Gflat2, shapes)])
 
         def step(k, arr=None):
-            st = L.ns5_bank(gp, dt, op, rows, cols, n_mats, NS_STEPS, ws_ptr, ws_bytes, sptr)
+            st = L.ns5_bank(gp if arr is None else arr, dt, op, rows, cols, n_mats, NS_STEPS, ws_ptr, ws_bytes,
+                            sptr)
             if st != 0:
                 raise muon.MuonError(st, "ns5_bank")
 
-        in_dev, in_host = Gflat, [Gflat.cpu().pin_memory()]
-        out_dev = Oflat
-        e2e_arr = None
+        e2e_in = [[Gflat], [Gflat2]]
+        e2e_host = [[Gflat.cpu().pin_memory()]]
+        e2e_out = [Oflat]
+
+        def e2e_step(j):
+            step(0, (gp, gp2)[j])
         gbytes = 2
 
     def barrier():
@@ -453,18 +521,13 @@ def main():
     muon.muon_set_debug("record_kernel_events", 0)
 
     # ------------------------------------------------------------- e2e
-    out_host = torch.empty(out_dev.numel(), dtype=out_dev.dtype).pin_memory()
+    out_host = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in e2e_out]
     e_steps = max(3, args.steps // 4)
     barrier()
-    e0.record(stream)
-    for k in range(e_steps):
-        in_dev.copy_(in_host[k % len(in_host)], non_blocking=True)
-        step(0, e2e_arr)
-        out_host.copy_(out_dev, non_blocking=True)
-    e1.record(stream)
+    e2e_ms = e2e_pipelined(stream, device, e_steps, e2e_in, e2e_host, e2e_step, e2e_out, out_host)
     barrier()
     clk = clocks.stop()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, world, device)
+    e2e_ms = max_over_ranks(e2e_ms, world, device)
     st = muon.muon_device_status(ws)
     if st != 0:
         raise muon.MuonError(st, "device status after timing")
@@ -531,8 +594,9 @@ def main():
         "kernels": kern,
         "e2e": {"value": n_total / (e2e_ms * 1e-3), "unit": "matrices/s",
                 "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": int(in_dev.numel() * in_dev.element_size()),
-                "d2h_bytes_per_step": int(out_dev.numel() * out_dev.element_size())},
+                "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in e2e_in[0])),
+                "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in e2e_out)),
+                "method": E2E_NOTE},
         "gpu_launches": int(sum(c for _, c in ktimes.values())),
         "gpu_launches_note": "kernels launched in the per-kernel timing pass (same count as the main timed loop)",
         "clocks": clk,
@@ -594,22 +658,24 @@ def run_adam(args, rank, world, device):
     barrier()
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, device)
 
-    # e2e: this step's gradients in from pinned host memory, parameters out
-    g_host = [g.cpu().pin_memory() for g in G]
+    # e2e: each step's gradients in from pinned host memory (two device
+    # gradient buffers), the updated parameters out
+    g_host = [[g.cpu().pin_memory() for g in G]]
     p_host = [torch.empty(p.shape, dtype=p.dtype).pin_memory() for p in P]
+    G2 = [torch.empty_like(g) for g in G]
+    Gsets = [G, G2]
     e_steps = max(3, args.steps // 4)
+    k0 = args.warmup + args.steps
+
+    def e2e_step(j):
+        muon.adam_step(P, Gsets[j], M, V, inputs.ADAM_STEP + k0, lr=hp["lr"], beta1=hp["beta1"],
+                       beta2=hp["beta2"], eps=hp["eps"], weight_decay=hp["weight_decay"],
+                       cautious=hp["cautious"], stream=stream)
     barrier()
-    e0.record(stream)
-    for k in range(e_steps):
-        for gd, gh in zip(G, g_host):
-            gd.copy_(gh, non_blocking=True)
-        step(args.warmup + args.steps + k)
-        for pd, ph in zip(P, p_host):
-            ph.copy_(pd, non_blocking=True)
-    e1.record(stream)
+    e2e_ms = e2e_pipelined(stream, device, e_steps, Gsets, g_host, e2e_step, P, p_host)
     barrier()
     clk = clocks.stop()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, world, device)
+    e2e_ms = max_over_ranks(e2e_ms, world, device)
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -638,7 +704,8 @@ def run_adam(args, rank, world, device):
                      "peak_source": f"{peak_src} (hbm_gbs)"},
         "e2e": {"value": n_total / (e2e_ms * 1e-3), "unit": "params/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": int(sum(g.numel() * g.element_size() for g in G)),
-                "d2h_bytes_per_step": int(sum(p.numel() * p.element_size() for p in P))},
+                "d2h_bytes_per_step": int(sum(p.numel() * p.element_size() for p in P)),
+                "method": E2E_NOTE},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
