@@ -107,8 +107,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   uint64_t* tfull = bars + 2 * kStages;        // accumulator ready (this CTA's lanes)
   uint64_t* tempty = bars + 2 * kStages + 2;   // leader: both CTAs drained it
   uint64_t* drain = bars + 2 * kStages + 4;
-  uint64_t* aux_full = bars + 2 * kStages + 5; // epilogue input tile landed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 6);
+  uint64_t* aux_full = bars + 2 * kStages + 5; // [2] epilogue input of a column half landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 7);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* never = reinterpret_cast<volatile int*>(tmem_slot + 2);  // stays 0
 
@@ -131,7 +131,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       ptx::mbar_init(ptx::smem_addr(&tempty[a]), 2 * kEpiWarps);
     }
     ptx::mbar_init(ptx::smem_addr(drain), 1);
-    ptx::mbar_init(ptx::smem_addr(aux_full), 1);
+    ptx::mbar_init(ptx::smem_addr(&aux_full[0]), 1);
+    ptx::mbar_init(ptx::smem_addr(&aux_full[1]), 1);
     *abort = 0;
     *never = 0;
     ptx::fence_mbar_init();
@@ -260,30 +261,46 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     // tile.  Warp w (2..9) reads lane quarter w % 4 (32 rows) and column half
     // (w - 2) / 4 (4 chunks of 32 columns).  The tile's 128 x 256 bf16 block
     // goes through the staging buffer: the epilogue input (A or X) arrives
-    // there by TMA, each thread reads its row's 16-byte pieces, writes the
-    // result in place, and one thread stores the block with TMA.  Gram and
-    // polynomial tiles above the diagonal also write their mirrored entries
-    // from registers, coalesced across the warp.
+    // there by TMA, each thread reads its row's 16-byte pieces and writes the
+    // result in place.  The two column halves (four warps, two 64-column
+    // boxes each) run independently, each with its own named barrier, input
+    // barrier and storing thread: a half stores its first box with TMA as
+    // soon as its four warps have written it (the store overlaps the second
+    // box), then its second box, and reloads both boxes for its next tile
+    // once the stores have read them.  Gram and polynomial tiles above the
+    // diagonal also write their mirrored entries from registers, coalesced
+    // across the warp.
     // The layout is TMA's 128-byte swizzle: boxes of 64 columns, rows of
     // 128 bytes, 16-byte piece j of row r at piece (j ^ (r % 8)).
     const int q = warp & 3;
     const int colhalf = (warp - 2) >> 2;
     const int row_local = q * 32 + lane;  // 0 .. 127 within this CTA's rows
-    const bool elected = warp == 2 && lane == 0;
+    const bool elected = warp == 2 && lane == 0;                  // diagnostics
+    const bool half_leader = warp == 2 + 4 * colhalf && lane == 0;  // stores / loads this half's boxes
+    const int half_bar = 2 + colhalf;                             // named barrier of this half
+    constexpr int kHalfThreads = 32 * kEpiWarps / 2;
+    uint64_t* my_aux = &aux_full[colhalf];
     const uint32_t stg_a = ptx::smem_addr(stg);
     const uint32_t tempty_leader[2] = {ptx::map_to_rank(ptx::smem_addr(&tempty[0]), 0),
                                        ptx::map_to_rank(ptx::smem_addr(&tempty[1]), 0)};
     const int rowoff = static_cast<int>(rank) * (kBM / 2);
-    auto load_aux = [&](int t) {
+    auto load_aux = [&](int t) {  // this half's two boxes of tile t's epilogue input
       const Tile tn = decode_tile<MODE>(P, t);
       const GemmClass& Cn = P.cls[tn.cls];
-      ptx::mbar_arrive_expect_tx(ptx::smem_addr(aux_full), kStageOut);
+      ptx::mbar_arrive_expect_tx(ptx::smem_addr(my_aux), kStageOut / 2);
 #pragma unroll
-      for (int bx = 0; bx < kBN / 64; ++bx)
-        ptx::tma_load_3d(stg_a + bx * (kBM / 2) * 128, &Cn.tmAux, ptx::smem_addr(aux_full), tn.J * kBN + 64 * bx,
+      for (int bb = 0; bb < 2; ++bb) {
+        const int bx = 2 * colhalf + bb;
+        ptx::tma_load_3d(stg_a + bx * (kBM / 2) * 128, &Cn.tmAux, ptx::smem_addr(my_aux), tn.J * kBN + 64 * bx,
                          tn.I * kBM + rowoff, tn.idx);
+      }
     };
-    if (MODE != kGram && elected && pair < P.total_tiles) load_aux(pair);
+    auto store_box = [&](const GemmClass& C, const Tile& tl, int bx) {
+      ptx::tma_store_3d(&C.tmOut, stg_a + bx * (kBM / 2) * 128, tl.J * kBN + 64 * bx, tl.I * kBM + rowoff,
+                        tl.idx);
+      ptx::bulk_commit();
+    };
+    if (MODE != kGram && half_leader && pair < P.total_tiles) load_aux(pair);
     uint32_t aux_phase = 0;
     bool ok = true;
     int it = 0;
@@ -293,7 +310,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
       if (MODE != kGram) {
-        if (!ptx::mbar_wait(ptx::smem_addr(aux_full), aux_phase, budget, abort)) {
+        if (!ptx::mbar_wait(ptx::smem_addr(my_aux), aux_phase, budget, abort)) {
           raise_timeout(P, abort);
           ok = false;
         }
@@ -347,19 +364,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           for (int e = 0; e < 4; ++e) w[ch][4 * jj + e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
           ptx::sts128(addr, w[ch][4 * jj], w[ch][4 * jj + 1], w[ch][4 * jj + 2], w[ch][4 * jj + 3]);
         }
-      }
-      // accumulator drained: the MMA warp may reuse it
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive_cluster(tempty_leader[acc]);
-      ptx::fence_async_smem();
-      ptx::named_sync(1, 32 * kEpiWarps);
-      if (elected) {
-#pragma unroll
-        for (int bx = 0; bx < kBN / 64; ++bx)
-          ptx::tma_store_3d(&C.tmOut, stg_a + bx * (kBM / 2) * 128, tl.J * kBN + 64 * bx, tl.I * kBM + rowoff,
-                            tl.idx);
-        ptx::bulk_commit();
+        if (ch == 3) {
+          // accumulator drained: the MMA warp may reuse it
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive_cluster(tempty_leader[acc]);
+        }
+        if (ch & 1) {
+          // box 2*colhalf + ch/2 written by the half's four warps: store it
+          ptx::fence_async_smem();
+          ptx::named_sync(half_bar, kHalfThreads);
+          if (half_leader) store_box(C, tl, 2 * colhalf + (ch >> 1));
+        }
       }
       if (MODE != kUpdate && tl.I != tl.J) {
         // mirrored entries (r, c) -> (c, r), straight from registers: a warp
@@ -379,23 +395,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           }
         }
       }
-      if (elected) {
-        ptx::bulk_wait_read0();  // staging free again
+      if (half_leader) {
+        ptx::bulk_wait_read0();  // this half's boxes are free again
         if (MODE != kGram && t + npairs < P.total_tiles) {
           ptx::fence_async_smem();
           load_aux(t + npairs);
         }
       }
-      ptx::named_sync(1, 32 * kEpiWarps);
+      ptx::named_sync(half_bar, kHalfThreads);
       if (prof && elected) {
         prof[kWpEpiBusy] += clock64() - w4;
         prof[kWpTiles] += 1;
       }
     }
-    if (elected) ptx::bulk_wait0();
-    if (MODE != kGram && elected && *abort) {
+    if (half_leader) ptx::bulk_wait0();
+    if (MODE != kGram && half_leader && *abort) {
       // an input tile may still be in flight
-      ptx::mbar_wait(ptx::smem_addr(aux_full), aux_phase, budget, never);
+      ptx::mbar_wait(ptx::smem_addr(my_aux), aux_phase, budget, never);
     }
   }
 
