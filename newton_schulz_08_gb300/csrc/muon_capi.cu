@@ -377,26 +377,26 @@ muon_status_t run(const std::vector<JobMat>& mats, const Plan& P, float lr, floa
           void* B = ws + cp.b_off;
           bool ok = true;
           // operands: A rows (box 64 x 128 per CTA), B rows or X columns;
-          // epilogue: input tile, output tile (64 x 128), mirrored block (64 x 256)
+          // epilogue: input and output boxes of one warp (64 x 32), mirrored block (64 x 256)
           if (mode == kGram) {
             ok = encode_map(&g.tmA, xs, cp.n, cp.m, cp.count, cp.ldx, kBK, kBM / 2) &&
                  encode_map(&g.tmB, xs, cp.n, cp.m, cp.count, cp.ldx, kBK, kBN / 2) &&
-                 encode_map(&g.tmAux, A, cp.m, cp.m, cp.count, cp.lda, 64, kBM / 2) &&
-                 encode_map(&g.tmOut, A, cp.m, cp.m, cp.count, cp.lda, 64, kBM / 2) &&
+                 encode_map(&g.tmAux, A, cp.m, cp.m, cp.count, cp.lda, 64, kEpiRows) &&
+                 encode_map(&g.tmOut, A, cp.m, cp.m, cp.count, cp.lda, 64, kEpiRows) &&
                  encode_map(&g.tmOutT, A, cp.m, cp.m, cp.count, cp.lda, 64, kBN);
             g.K = cp.n;
           } else if (mode == kPoly) {
             ok = encode_map(&g.tmA, A, cp.m, cp.m, cp.count, cp.lda, kBK, kBM / 2) &&
                  encode_map(&g.tmB, A, cp.m, cp.m, cp.count, cp.lda, kBK, kBN / 2) &&
-                 encode_map(&g.tmAux, A, cp.m, cp.m, cp.count, cp.lda, 64, kBM / 2) &&
-                 encode_map(&g.tmOut, B, cp.m, cp.m, cp.count, cp.lda, 64, kBM / 2) &&
+                 encode_map(&g.tmAux, A, cp.m, cp.m, cp.count, cp.lda, 64, kEpiRows) &&
+                 encode_map(&g.tmOut, B, cp.m, cp.m, cp.count, cp.lda, 64, kEpiRows) &&
                  encode_map(&g.tmOutT, B, cp.m, cp.m, cp.count, cp.lda, 64, kBN);
             g.K = cp.m;
           } else {
             ok = encode_map(&g.tmA, B, cp.m, cp.m, cp.count, cp.lda, kBK, kBM / 2) &&
                  encode_map(&g.tmB, xs, cp.n, cp.m, cp.count, cp.ldx, 64, kBK) &&
-                 encode_map(&g.tmAux, xs, cp.n, cp.m, cp.count, cp.ldx, 64, kBM / 2) &&
-                 encode_map(&g.tmOut, xd, cp.n, cp.m, cp.count, cp.ldx, 64, kBM / 2) &&
+                 encode_map(&g.tmAux, xs, cp.n, cp.m, cp.count, cp.ldx, 64, kEpiRows) &&
+                 encode_map(&g.tmOut, xd, cp.n, cp.m, cp.count, cp.ldx, 64, kEpiRows) &&
                  encode_map(&g.tmOutT, xd, cp.n, cp.m, cp.count, cp.ldx, 64, kBM / 2);
             g.K = cp.m;
           }

@@ -107,8 +107,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   uint64_t* tfull = bars + 2 * kStages;        // accumulator ready (this CTA's lanes)
   uint64_t* tempty = bars + 2 * kStages + 2;   // leader: both CTAs drained it
   uint64_t* drain = bars + 2 * kStages + 4;
-  uint64_t* aux_full = bars + 2 * kStages + 5; // [2] epilogue input of a column half landed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 7);
+  uint64_t* aux_full = bars + 2 * kStages + 5; // [kEpiWarps] epilogue input of a warp landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5 + kEpiWarps);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* never = reinterpret_cast<volatile int*>(tmem_slot + 2);  // stays 0
 
@@ -131,8 +131,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       ptx::mbar_init(ptx::smem_addr(&tempty[a]), 2 * kEpiWarps);
     }
     ptx::mbar_init(ptx::smem_addr(drain), 1);
-    ptx::mbar_init(ptx::smem_addr(&aux_full[0]), 1);
-    ptx::mbar_init(ptx::smem_addr(&aux_full[1]), 1);
+    for (int w = 0; w < kEpiWarps; ++w) ptx::mbar_init(ptx::smem_addr(&aux_full[w]), 1);
     *abort = 0;
     *never = 0;
     ptx::fence_mbar_init();
@@ -262,45 +261,43 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     // (w - 2) / 4 (4 chunks of 32 columns).  The tile's 128 x 256 bf16 block
     // goes through the staging buffer: the epilogue input (A or X) arrives
     // there by TMA, each thread reads its row's 16-byte pieces and writes the
-    // result in place.  The two column halves (four warps, two 64-column
-    // boxes each) run independently, each with its own named barrier, input
-    // barrier and storing thread: a half stores its first box with TMA as
-    // soon as its four warps have written it (the store overlaps the second
-    // box), then its second box, and reloads both boxes for its next tile
-    // once the stores have read them.  Gram and polynomial tiles above the
-    // diagonal also write their mirrored entries from registers, coalesced
-    // across the warp.
+    // result in place.  Every warp works alone: its 32 rows of each of its
+    // two 64-column boxes form a TMA box of their own (32 rows of 128 bytes,
+    // 1 KB aligned, so the swizzle phase is that of the full box), which
+    // lane 0 stores as soon as the warp has written it (the first store
+    // overlaps the second box) and reloads for the warp's next tile once the
+    // store has read it, on the warp's own input barrier.  No barrier spans
+    // warps.  Gram and polynomial tiles above the diagonal also write their
+    // mirrored entries from registers, coalesced across the warp.
     // The layout is TMA's 128-byte swizzle: boxes of 64 columns, rows of
     // 128 bytes, 16-byte piece j of row r at piece (j ^ (r % 8)).
     const int q = warp & 3;
     const int colhalf = (warp - 2) >> 2;
     const int row_local = q * 32 + lane;  // 0 .. 127 within this CTA's rows
-    const bool elected = warp == 2 && lane == 0;                  // diagnostics
-    const bool half_leader = warp == 2 + 4 * colhalf && lane == 0;  // stores / loads this half's boxes
-    const int half_bar = 2 + colhalf;                             // named barrier of this half
-    constexpr int kHalfThreads = 32 * kEpiWarps / 2;
-    uint64_t* my_aux = &aux_full[colhalf];
+    const bool elected = warp == 2 && lane == 0;  // diagnostics
+    uint64_t* my_aux = &aux_full[warp - 2];
+    const uint32_t my_rows = static_cast<uint32_t>(q * kEpiRows * 128);  // this warp's rows within a box
     const uint32_t stg_a = ptx::smem_addr(stg);
     const uint32_t tempty_leader[2] = {ptx::map_to_rank(ptx::smem_addr(&tempty[0]), 0),
                                        ptx::map_to_rank(ptx::smem_addr(&tempty[1]), 0)};
     const int rowoff = static_cast<int>(rank) * (kBM / 2);
-    auto load_aux = [&](int t) {  // this half's two boxes of tile t's epilogue input
+    auto load_aux = [&](int t) {  // this warp's rows of its two boxes of tile t's epilogue input
       const Tile tn = decode_tile<MODE>(P, t);
       const GemmClass& Cn = P.cls[tn.cls];
-      ptx::mbar_arrive_expect_tx(ptx::smem_addr(my_aux), kStageOut / 2);
+      ptx::mbar_arrive_expect_tx(ptx::smem_addr(my_aux), 2 * kEpiRows * 128);
 #pragma unroll
       for (int bb = 0; bb < 2; ++bb) {
         const int bx = 2 * colhalf + bb;
-        ptx::tma_load_3d(stg_a + bx * (kBM / 2) * 128, &Cn.tmAux, ptx::smem_addr(my_aux), tn.J * kBN + 64 * bx,
-                         tn.I * kBM + rowoff, tn.idx);
+        ptx::tma_load_3d(stg_a + bx * (kBM / 2) * 128 + my_rows, &Cn.tmAux, ptx::smem_addr(my_aux),
+                         tn.J * kBN + 64 * bx, tn.I * kBM + rowoff + q * kEpiRows, tn.idx);
       }
     };
     auto store_box = [&](const GemmClass& C, const Tile& tl, int bx) {
-      ptx::tma_store_3d(&C.tmOut, stg_a + bx * (kBM / 2) * 128, tl.J * kBN + 64 * bx, tl.I * kBM + rowoff,
-                        tl.idx);
+      ptx::tma_store_3d(&C.tmOut, stg_a + bx * (kBM / 2) * 128 + my_rows, tl.J * kBN + 64 * bx,
+                        tl.I * kBM + rowoff + q * kEpiRows, tl.idx);
       ptx::bulk_commit();
     };
-    if (MODE != kGram && half_leader && pair < P.total_tiles) load_aux(pair);
+    if (MODE != kGram && lane == 0 && pair < P.total_tiles) load_aux(pair);
     uint32_t aux_phase = 0;
     bool ok = true;
     int it = 0;
@@ -321,8 +318,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         raise_timeout(P, abort);
         ok = false;
       }
-      // all epilogue threads must agree on leaving (named barriers follow)
-      if (ptx::named_sync_or(1, 32 * kEpiWarps, !ok || *abort)) break;
+      // the warp's lanes agree on leaving (warp-level syncs follow)
+      if (__any_sync(0xFFFFFFFFu, !ok || *abort)) break;
       const long long w4 = (prof && elected) ? clock64() : 0;
       if (prof && elected) prof[kWpEpiTfull] += w4 - w3;
       ptx::tc_fence_after();
@@ -371,10 +368,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           if (lane == 0) ptx::mbar_arrive_cluster(tempty_leader[acc]);
         }
         if (ch & 1) {
-          // box 2*colhalf + ch/2 written by the half's four warps: store it
+          // this warp's rows of box 2*colhalf + ch/2 are written: store them
           ptx::fence_async_smem();
-          ptx::named_sync(half_bar, kHalfThreads);
-          if (half_leader) store_box(C, tl, 2 * colhalf + (ch >> 1));
+          __syncwarp();
+          if (lane == 0) store_box(C, tl, 2 * colhalf + (ch >> 1));
         }
       }
       if (MODE != kUpdate && tl.I != tl.J) {
@@ -395,21 +392,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           }
         }
       }
-      if (half_leader) {
-        ptx::bulk_wait_read0();  // this half's boxes are free again
+      if (lane == 0) {
+        ptx::bulk_wait_read0();  // this warp's rows are free again
         if (MODE != kGram && t + npairs < P.total_tiles) {
           ptx::fence_async_smem();
           load_aux(t + npairs);
         }
       }
-      ptx::named_sync(half_bar, kHalfThreads);
+      __syncwarp();
       if (prof && elected) {
         prof[kWpEpiBusy] += clock64() - w4;
         prof[kWpTiles] += 1;
       }
     }
-    if (half_leader) ptx::bulk_wait0();
-    if (MODE != kGram && half_leader && *abort) {
+    if (lane == 0) ptx::bulk_wait0();
+    if (MODE != kGram && lane == 0 && *abort) {
       // an input tile may still be in flight
       ptx::mbar_wait(ptx::smem_addr(my_aux), aux_phase, budget, never);
     }

@@ -154,6 +154,7 @@ constexpr int kStageBytes = kStageA + kStageB;
 constexpr int kStageOut = (kBM / 2) * kBN * 2;  // 64 KB epilogue staging
 constexpr int kGemmSmem = kStages * kStageBytes + kStageOut + 1024 /*align*/ + 256 /*barriers*/;
 constexpr int kEpiWarps = 8;     // two warps per TMEM lane quarter, one per column half
+constexpr int kEpiRows = 32;     // rows of an epilogue staging box: one warp's TMEM lane quarter
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 
 }  // namespace muon
