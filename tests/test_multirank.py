@@ -1,8 +1,10 @@
 """The step on several processes: the work-balanced partition of a bank
-(muon_partition, host only) and the way bench.py splits a world-sized bank
-and aggregates its timing.  CPU only: the multi-rank test runs two `gloo`
-ranks as child processes, each computing its own matrices with the oracle
-(standing in for the GPU step, which the ranks never exchange data for).
+(muon_partition, host only), the way bench.py splits a world-sized bank and
+aggregates its timing, and the exchange of the sharded data-parallel step
+(gradients averaged onto owners, parameters broadcast from owners).  The
+multi-rank tests run two `gloo` ranks on CPU as child processes, each
+computing its own matrices with the oracle standing in for the GPU step; one
+GPU test runs sharded_muon_step itself over a one-rank NCCL group.
 
 The page "深入解析KellerJordan/modded-nanogpt中的训练架构与优化技术"
 (reposource.net), section "Muon优化器：动量正交化技术", shards the step by
@@ -144,3 +146,79 @@ def test_two_gloo_ranks_share_a_world_sized_bank(L):
     ref = [_oracle_step(g, full[g]) for g in range(total)]
     np.testing.assert_array_equal(p, np.concatenate([r[0].ravel() for r in ref]))
     np.testing.assert_array_equal(buf, np.concatenate([r[1].ravel() for r in ref]))
+
+
+# ------------------------------------------------ sharded data-parallel step
+def _sharded_worker(rank, world, port, out_dir):
+    """The exchange of sharded_muon_step around the local step, on CPU
+    tensors: gradients averaged onto owners, the owner's step (the oracle
+    stands in for the CUDA step here), parameters broadcast from owners."""
+    import torch
+    import torch.distributed as dist
+
+    from newton_schulz_08_gb300 import inputs, sharded
+    from oracle import muon_step
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        params = [torch.from_numpy(inputs.param(s, i)) for i, s in enumerate(SMALL_BANK)]
+        grads = [torch.from_numpy(inputs.grad(s, i, step=rank)) for i, s in enumerate(SMALL_BANK)]
+        bufs = [torch.from_numpy(inputs.buffer(s, i)) for i, s in enumerate(SMALL_BANK)]
+        owner = sharded.owners([p.shape for p in params], world)
+        mine = sharded.reduce_grads_to_owners(grads, owner, rank, world)
+        assert sorted(mine) == [i for i, o in enumerate(owner) if o == rank]
+        for i, g in mine.items():
+            new_p, _, _ = muon_step(params[i].numpy(), g.numpy(), bufs[i].numpy(), 0.02, 0.95, True, 5, "fp64")
+            params[i].copy_(torch.from_numpy(new_p.astype(np.float32)))
+        sharded.broadcast_params_from_owners(params, owner, world)
+        np.save(os.path.join(out_dir, f"p{rank}.npy"), np.concatenate([p.numpy().ravel() for p in params]))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_sharded_step_exchange_on_two_gloo_ranks(L):
+    import torch.multiprocessing as mp
+
+    from newton_schulz_08_gb300 import inputs
+    from oracle import muon_step
+    with tempfile.TemporaryDirectory() as d:
+        mp.spawn(_sharded_worker, args=(WORKERS, _free_port(), d), nprocs=WORKERS, join=True)
+        got = [np.load(os.path.join(d, f"p{r}.npy")) for r in range(WORKERS)]
+    # every rank ends with the same parameters ...
+    np.testing.assert_array_equal(got[0], got[1])
+    # ... equal to one process stepping every matrix with the averaged gradient
+    ref = []
+    for i, s in enumerate(SMALL_BANK):
+        g = (inputs.grad(s, i, step=0) + inputs.grad(s, i, step=1)) / np.float32(WORKERS)
+        new_p, _, _ = muon_step(inputs.param(s, i), g, inputs.buffer(s, i), 0.02, 0.95, True, 5, "fp64")
+        ref.append(new_p.astype(np.float32).ravel())
+    np.testing.assert_array_equal(got[0], np.concatenate(ref))
+
+
+@pytest.mark.gpu
+def test_sharded_step_on_one_nccl_rank_equals_muon_step():
+    """sharded_muon_step with world size 1: the fp32-averaged gradient has the
+    bf16 gradient's values, so the result equals muon_step bit for bit."""
+    import torch
+    import torch.distributed as dist
+
+    from newton_schulz_08_gb300 import inputs, sharded
+    shapes = [(256, 256), (300, 100), (100, 300), (768, 768)]
+    dev = torch.device("cuda")
+    mk = lambda f: [torch.from_numpy(f(s, i)).to(dev) for i, s in enumerate(shapes)]
+    P1, B1 = mk(inputs.param), mk(inputs.buffer)
+    P2, B2 = [p.clone() for p in P1], [b.clone() for b in B1]
+    G = [g.to(torch.bfloat16) for g in mk(inputs.grad)]
+    store = dist.TCPStore("127.0.0.1", _free_port(), 1, True)
+    dist.init_process_group("nccl", store=store, rank=0, world_size=1)
+    try:
+        ws = sharded.sharded_muon_step(P1, G, B1)
+        torch.cuda.synchronize()
+        assert muon.muon_device_status(ws) == muon.MUON_OK
+    finally:
+        dist.destroy_process_group()
+    muon.muon_step(P2, G, B2)
+    torch.cuda.synchronize()
+    for a, b in zip(P1 + B1, P2 + B2):
+        assert torch.equal(a, b)
