@@ -289,3 +289,34 @@ def test_resume_matches_straight_run():
 def test_empty_calls():
     assert muon.ns5(torch.empty((0, 8, 8), device="cuda"), 5).shape == (0, 8, 8)
     assert muon.ns5_bank([], 5) == []
+
+
+def test_cuda_graph_capture_replays_the_step():
+    """muon_step under stream capture (cluster launches, programmatic
+    dependent launch, the status memset): replaying the captured step three
+    times gives the eager result bit for bit."""
+    shapes = [(256, 256), (300, 100), (100, 300), (129, 257)]
+    rng = np.random.default_rng(21)
+    P0 = [to_dev(rng.standard_normal(s).astype(np.float32) * np.float32(0.02)) for s in shapes]
+    G = [to_dev(rng.standard_normal(s).astype(np.float32) * np.float32(1e-3), torch.bfloat16) for s in shapes]
+    B0 = [to_dev(rng.standard_normal(s).astype(np.float32) * np.float32(1e-3)) for s in shapes]
+    P, B = [p.clone() for p in P0], [b.clone() for b in B0]
+    ws = muon.muon_step(P, G, B)  # plan, attributes and workspace set up outside the capture
+    for x, x0 in zip(P + B, P0 + B0):
+        x.copy_(x0)
+    for _ in range(3):
+        muon.muon_step(P, G, B, workspace=ws)
+    want = [x.clone() for x in P + B]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        muon.muon_step(P, G, B, workspace=ws)
+    for x, x0 in zip(P + B, P0 + B0):
+        x.copy_(x0)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    check_status(ws)
+    for a, b in zip(P + B, want):
+        assert torch.equal(a, b)
