@@ -100,15 +100,16 @@ template <int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* stg = smem + kStages * kStageBytes;  // epilogue staging tile
-  uint64_t* bars = reinterpret_cast<uint64_t*>(stg + kStageOut);
+  constexpr int kSt = GemmShape<MODE>::stages;
+  uint8_t* stg = smem + kSt * kStageBytes;  // epilogue staging tile
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stg + GemmShape<MODE>::staging);
   uint64_t* full = bars;                       // leader: both CTAs' tiles landed
-  uint64_t* empty = bars + kStages;            // stage free in this CTA
-  uint64_t* tfull = bars + 2 * kStages;        // accumulator ready (this CTA's lanes)
-  uint64_t* tempty = bars + 2 * kStages + 2;   // leader: both CTAs drained it
-  uint64_t* drain = bars + 2 * kStages + 4;
-  uint64_t* aux_full = bars + 2 * kStages + 5; // [kEpiWarps] epilogue input of a warp landed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5 + kEpiWarps);
+  uint64_t* empty = bars + kSt;            // stage free in this CTA
+  uint64_t* tfull = bars + 2 * kSt;        // accumulator ready (this CTA's lanes)
+  uint64_t* tempty = bars + 2 * kSt + 2;   // leader: both CTAs drained it
+  uint64_t* drain = bars + 2 * kSt + 4;
+  uint64_t* aux_full = bars + 2 * kSt + 5; // [kEpiWarps] epilogue input of a warp landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kSt + 5 + kEpiWarps);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* never = reinterpret_cast<volatile int*>(tmem_slot + 2);  // stays 0
 
@@ -122,7 +123,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   const int npairs = static_cast<int>(ptx::nclusters_x());
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kSt; ++s) {
       ptx::mbar_init(ptx::smem_addr(&full[s]), 1);
       ptx::mbar_init(ptx::smem_addr(&empty[s]), 1);
     }
@@ -192,7 +193,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           } else {
             ptx::tma_load_3d_pair(sb, &C.tmB, fb, kb * kBK, tl.J * kBN + half, tl.idx);
           }
-          if (++stage == kStages) {
+          if (++stage == kSt) {
             stage = 0;
             phase ^= 1;
           }
@@ -241,7 +242,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
             ptx::mma_bf16_pair(d, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
           }
           ptx::mma_commit_pair_mc(ptx::smem_addr(&empty[stage]), 0x3);
-          if (++stage == kStages) {
+          if (++stage == kSt) {
             stage = 0;
             phase ^= 1;
           }
@@ -293,7 +294,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       }
     };
     auto store_box = [&](const GemmClass& C, const Tile& tl, int bx) {
-      ptx::tma_store_3d(&C.tmOut, stg_a + bx * (kBM / 2) * 128 + my_rows, tl.J * kBN + 64 * bx,
+      const int sbx = MODE == kGram ? colhalf : bx;
+      ptx::tma_store_3d(&C.tmOut, stg_a + sbx * (kBM / 2) * 128 + my_rows, tl.J * kBN + 64 * bx,
                         tl.I * kBM + rowoff + q * kEpiRows, tl.idx);
       ptx::bulk_commit();
     };
@@ -332,7 +334,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         ptx::tmem_ld32(tb + ch * 32, r);
         ptx::tmem_ld_wait();
         const int c0 = colhalf * (kBN / 2) + ch * 32;  // column within the tile
-        const uint32_t rowa = stg_a + (c0 >> 6) * ((kBM / 2) * 128) + row_local * 128;
+        // staging box: the tile's 64-column box, or (Gram) the warp's one box
+        const int sbx = MODE == kGram ? colhalf : (c0 >> 6);
+        const uint32_t rowa = stg_a + sbx * ((kBM / 2) * 128) + row_local * 128;
+        if (MODE == kGram && ch == 2) {
+          // the warp's box still holds its first half until the store has read it
+          if (lane == 0) ptx::bulk_wait_read0();
+          __syncwarp();
+        }
         const int j0 = (c0 & 63) >> 3;
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
@@ -440,10 +449,12 @@ cudaError_t launch_ns_gemm(int mode, const GemmParams& P, int num_sms, cudaStrea
   const void* fn = mode == kGram   ? reinterpret_cast<const void*>(&ns_gemm_kernel<kGram>)
                    : mode == kPoly ? reinterpret_cast<const void*>(&ns_gemm_kernel<kPoly>)
                                    : reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate>);
+  const int smem = mode == kGram ? GemmShape<kGram>::smem : mode == kPoly ? GemmShape<kPoly>::smem
+                                                                         : GemmShape<kUpdate>::smem;
   static int max_pairs[3] = {0, 0, 0};
   cudaError_t e = cudaSuccess;
   if (max_pairs[mode] <= 0) {
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
   }
   cudaLaunchAttribute attr[2];
@@ -455,7 +466,7 @@ cudaError_t launch_ns_gemm(int mode, const GemmParams& P, int num_sms, cudaStrea
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kGemmThreads);
-  cfg.dynamicSmemBytes = kGemmSmem;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;

@@ -153,6 +153,17 @@ constexpr int kStageB = (kBN / 2) * kBK * 2;  // 16 KB
 constexpr int kStageBytes = kStageA + kStageB;
 constexpr int kStageOut = (kBM / 2) * kBN * 2;  // 64 KB epilogue staging
 constexpr int kGemmSmem = kStages * kStageBytes + kStageOut + 1024 /*align*/ + 256 /*barriers*/;
+
+// Shared-memory shape per phase.  A Gram tile has no epilogue input, so its
+// staging holds one 64 x 32 box per warp (32 KB, reused for the warp's second
+// box once the first has been stored) and the space freed is a sixth operand
+// stage; the polynomial and update tiles stage the input next to the output.
+template <int MODE>
+struct GemmShape {
+  static constexpr int stages = MODE == kGram ? kStages + 1 : kStages;
+  static constexpr int staging = MODE == kGram ? kStageOut / 2 : kStageOut;
+  static constexpr int smem = stages * kStageBytes + staging + 1024 /*align*/ + 256 /*barriers*/;
+};
 constexpr int kEpiWarps = 8;     // two warps per TMEM lane quarter, one per column half
 constexpr int kEpiRows = 32;     // rows of an epilogue staging box: one warp's TMEM lane quarter
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
