@@ -27,7 +27,7 @@
 
 namespace muon {
 
-cudaError_t launch_ns_gemm(int mode, const GemmParams& P, int num_sms, cudaStream_t stream);
+cudaError_t launch_ns_gemm(int mode, int sym, const GemmParams& P, int num_sms, cudaStream_t stream);
 cudaError_t launch_momentum_cast(const K1Params& P, int blocks, cudaStream_t stream);
 cudaError_t launch_normalise(const NormParams& P, int blocks, cudaStream_t stream);
 cudaError_t launch_apply(const ApplyParams& P, int blocks, cudaStream_t stream);
@@ -268,6 +268,25 @@ bool encode_map(CUtensorMap* map, void* base, int cols, int rows, int count, int
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D bf16 map viewing the columns of `count` matrices of rows x cols (row
+// pitch `pitch`) as 64-column chunks: dims (64, rows, cols / 64, count),
+// box (64, 64, 2, 1).  A copy brings two 64-column swizzle atoms of 64 rows,
+// one after the other, as an MN-major operand needs them.  Only for cols a
+// multiple of 64 (a chunk never reaches past a row).
+bool encode_map4(CUtensorMap* map, void* base, int cols, int rows, int count, int pitch) {
+  auto enc = tensor_map_encoder();
+  if (!enc || cols % 64 != 0) return false;
+  cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols / 64),
+                        static_cast<cuuint64_t>(count)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(pitch) * 2, 128,
+                           static_cast<cuuint64_t>(pitch) * 2 * static_cast<cuuint64_t>(rows)};
+  cuuint32_t box[4] = {64, 64, 2, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // square kBM x kBN tiles on and above the diagonal
 int sym_tiles_per_mat(int m) {
   const int tn = static_cast<int>(ceil_div(m, kBN));
@@ -364,43 +383,51 @@ muon_status_t run(const std::vector<JobMat>& mats, const Plan& P, float lr, floa
     const int src = t & 1, dst = src ^ 1;
     for (size_t c0 = 0; c0 < P.cls.size(); c0 += kMaxClasses) {
       const int nc = static_cast<int>(std::min<size_t>(kMaxClasses, P.cls.size() - c0));
+      // Gram and polynomial: classes whose A is stored block-upper (m up to
+      // kSymUpperMaxM) and the others go to separate kernel instantiations
       for (int mode = kGram; mode <= kUpdate; ++mode) {
+       for (int sym = 0; sym <= (mode == kUpdate ? 0 : 1); ++sym) {
         GemmParams gp;
         std::memset(&gp, 0, sizeof(gp));
         int tiles = 0;
+        int ng = 0;
         for (int j = 0; j < nc; ++j) {
           const ClassPlan& cp = P.cls[c0 + j];
-          GemmClass& g = gp.cls[j];
+          if (mode != kUpdate && (cp.m <= kSymUpperMaxM ? 1 : 0) != sym) continue;
+          GemmClass& g = gp.cls[ng++];
           void* xs = ws + cp.x_off[src];
           void* xd = ws + cp.x_off[dst];
           void* A = ws + cp.a_off;
           void* B = ws + cp.b_off;
           bool ok = true;
-          // operands: A rows (box 64 x 128 per CTA), B rows or X columns;
-          // epilogue: input and output boxes of one warp (64 x 32), mirrored block (64 x 256)
+          // operands: A rows (box 64 x 128 per CTA), B rows or X columns, and
+          // the symmetric operand's stored blocks read transposed (64 x 64);
+          // epilogue: input and output boxes of one warp (64 x 32)
           if (mode == kGram) {
             ok = encode_map(&g.tmA, xs, cp.n, cp.m, cp.count, cp.ldx, kBK, kBM / 2) &&
                  encode_map(&g.tmB, xs, cp.n, cp.m, cp.count, cp.ldx, kBK, kBN / 2) &&
                  encode_map(&g.tmAux, A, cp.m, cp.m, cp.count, cp.lda, 64, kEpiRows) &&
                  encode_map(&g.tmOut, A, cp.m, cp.m, cp.count, cp.lda, 64, kEpiRows) &&
-                 encode_map(&g.tmOutT, A, cp.m, cp.m, cp.count, cp.lda, 64, kBN);
+                 encode_map(&g.tmT, A, cp.m, cp.m, cp.count, cp.lda, 64, kBK);
             g.K = cp.n;
           } else if (mode == kPoly) {
             ok = encode_map(&g.tmA, A, cp.m, cp.m, cp.count, cp.lda, kBK, kBM / 2) &&
                  encode_map(&g.tmB, A, cp.m, cp.m, cp.count, cp.lda, kBK, kBN / 2) &&
                  encode_map(&g.tmAux, A, cp.m, cp.m, cp.count, cp.lda, 64, kEpiRows) &&
                  encode_map(&g.tmOut, B, cp.m, cp.m, cp.count, cp.lda, 64, kEpiRows) &&
-                 encode_map(&g.tmOutT, B, cp.m, cp.m, cp.count, cp.lda, 64, kBN);
+                 encode_map(&g.tmT, A, cp.m, cp.m, cp.count, cp.lda, 64, kBK);
             g.K = cp.m;
           } else {
             ok = encode_map(&g.tmA, B, cp.m, cp.m, cp.count, cp.lda, kBK, kBM / 2) &&
                  encode_map(&g.tmB, xs, cp.n, cp.m, cp.count, cp.ldx, 64, kBK) &&
                  encode_map(&g.tmAux, xs, cp.n, cp.m, cp.count, cp.ldx, 64, kEpiRows) &&
                  encode_map(&g.tmOut, xd, cp.n, cp.m, cp.count, cp.ldx, 64, kEpiRows) &&
-                 encode_map(&g.tmOutT, xd, cp.n, cp.m, cp.count, cp.ldx, 64, kBM / 2);
+                 encode_map(&g.tmT, B, cp.m, cp.m, cp.count, cp.lda, 64, kBK);
             g.K = cp.m;
           }
           if (!ok) return MUON_ERR_CUDA;
+          // poly: one-copy transposed reads of A where the width allows
+          g.t4 = mode == kPoly && sym && encode_map4(&g.tmT4, A, cp.m, cp.m, cp.count, cp.lda);
           g.out = static_cast<__nv_bfloat16*>(mode == kGram ? A : B);
           g.ld_out = cp.lda;
           g.out_mat_stride = static_cast<long long>(cp.m) * cp.lda;
@@ -419,7 +446,8 @@ muon_status_t run(const std::vector<JobMat>& mats, const Plan& P, float lr, floa
           g.mat_begin = cp.mat_begin;
           tiles += g.tiles_per_mat * cp.count;
         }
-        gp.n_classes = nc;
+        if (ng == 0) continue;
+        gp.n_classes = ng;
         gp.total_tiles = tiles;
         gp.ca = kCoefA;
         gp.cb = kCoefB;
@@ -430,8 +458,9 @@ muon_status_t run(const std::vector<JobMat>& mats, const Plan& P, float lr, floa
         gp.wait_profile = reinterpret_cast<long long*>(g_wait_profile.load());
         EventPair ev;
         const bool rec = ev_begin(ev, 2 + mode, stream);
-        if (launch_ns_gemm(mode, gp, sms, stream) != cudaSuccess) return MUON_ERR_CUDA;
+        if (launch_ns_gemm(mode, sym, gp, sms, stream) != cudaSuccess) return MUON_ERR_CUDA;
         ev_end(ev, rec, stream);
+       }
       }
     }
   }

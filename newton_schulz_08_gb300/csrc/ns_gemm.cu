@@ -7,33 +7,43 @@
 // with X an m x n bfloat16 matrix (m <= n) and (a, b, c) = (3.4445, -4.7750,
 // 2.0315).  Each statement's result is rounded once to bfloat16.
 //
-//   kGram   : A = X X^T.          Only tiles holding upper-triangle entries are
-//             computed; the epilogue writes each entry with r <= c to (r, c)
-//             and, mirrored, to (c, r), so A is exactly symmetric.
+//   kGram   : A = X X^T.          Only the 256 x 256 blocks on and above the
+//             diagonal are computed (diagonal blocks whole: the tensor core's
+//             sums for (r, c) and (c, r) agree bit for bit, so A is exactly
+//             symmetric).  For m up to kSymUpperMaxM only those blocks are
+//             stored and the polynomial reads the others transposed; for
+//             wider A the epilogue also writes the mirrored entries.
 //   kPoly   : B = b A + c (A A).  A is symmetric, so A A = A A^T and the same
-//             upper-triangle Gram structure applies with K = m; the epilogue
-//             reads A's tile and fuses b A + c (.).
+//             block-upper structure applies with K = m.  Where A is stored
+//             block-upper, operand blocks below the diagonal are loaded from
+//             the stored block above it as MN-major operands (one 4-D copy
+//             per 128 x 64 half where the width is a multiple of 64).  The
+//             epilogue reads A's (upper) tile, fuses b A + c (.), and also
+//             writes the mirrored entries, so B is stored whole.
 //   kUpdate : X' = a X + B X.     All tiles of the m x n result; B is the
-//             K-major operand, X the MN-major one.  The epilogue reads X's
-//             tile and fuses a X + (.).  (The parameter update after the
-//             last step is a separate coalesced pass, apply_kernel.)
+//             K-major A operand, X the MN-major B operand.  The epilogue
+//             reads X's tile and fuses a X + (.).  (The parameter update
+//             after the last step is a separate coalesced pass, apply_kernel.)
 //
 // Kernel structure: clusters of two CTAs on neighbouring SMs; each pair
 // computes 256 x 256 output tiles with tcgen05.mma.cta_group::2 (M = 256 over
 // the pair), persistent over a static tile list that spans all shape classes
 // of the bank.  Per CTA:
-//   warp 0     TMA producer: 6-stage ring of this CTA's halves, (128 x 64) A
-//              rows and (128 x 64) B columns, 128-byte swizzle; completion is
-//              counted on the leader CTA's full barrier.
+//   warp 0     TMA producer: 5-stage ring (6 for the Gram, whose epilogue
+//              stages no input) of this CTA's halves, (128 x 64) A rows and
+//              (128 x 64) B columns, 128-byte swizzle; completion is counted
+//              on the leader CTA's full barrier.
 //   warp 1     TMEM allocation (both CTAs, 2 x 256 fp32 accumulator columns);
 //              in the leader CTA one thread issues the MMAs 256 x 256 x 16
-//              and commits to the stage / accumulator barriers of both CTAs.
+//              (operand major-ness chosen per K block in the polynomial) and
+//              commits to the
+//              stage / accumulator barriers of both CTAs.
 //   warps 2-9  epilogue of this CTA's 128 accumulator rows: two warps per
-//              TMEM lane quarter, each owning half of the 256 columns; the
-//              epilogue input row (A or X) is loaded before the accumulator
-//              is ready, then tcgen05.ld of 32 columns at a time, fused
-//              arithmetic, bf16 rounding, stores; finally an arrive on the
-//              leader's accumulator-empty barrier.
+//              TMEM lane quarter, each owning half of the 256 columns and
+//              working alone (its own TMA boxes and input barrier):
+//              tcgen05.ld of 32 columns at a time, fused arithmetic, bf16
+//              rounding, staged stores; an arrive on the leader's
+//              accumulator-empty barrier once its columns are read.
 // Each CTA moves 32 KB per 64-deep K block for 2 x 128 x 256 x 64 MACs of
 // the pair: a third less operand traffic per FLOP than single-CTA
 // 128 x 256 tiles.  Every barrier wait is bounded; on expiry the CTA raises
@@ -96,7 +106,12 @@ __device__ __forceinline__ float word_hi(uint32_t w) { return __uint_as_float(w 
 
 }  // namespace
 
-template <int MODE>
+// SYM (Gram and polynomial only): 1 for classes whose A is stored as its
+// blocks on and above the diagonal only (m <= kSymUpperMaxM): the Gram writes
+// no mirrored entries and the polynomial reads the blocks below the diagonal
+// transposed.  A compile-time choice, so that the other classes run code
+// without any of it.
+template <int MODE, int SYM>
 __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -162,7 +177,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         ptx::prefetch_tmap(&P.cls[c].tmB);
         ptx::prefetch_tmap(&P.cls[c].tmAux);
         ptx::prefetch_tmap(&P.cls[c].tmOut);
-        ptx::prefetch_tmap(&P.cls[c].tmOutT);
+        ptx::prefetch_tmap(&P.cls[c].tmT);
+        ptx::prefetch_tmap(&P.cls[c].tmT4);
       }
       int stage = 0;
       uint32_t phase = 0;
@@ -184,12 +200,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           const uint32_t sa = ptx::smem_addr(smem + stage * kStageBytes);
           const uint32_t sb = sa + kStageA;
           if (rank == 0) ptx::mbar_arrive_expect_tx(ptx::smem_addr(&full[stage]), 2 * kStageBytes);
-          ptx::tma_load_3d_pair(sa, &C.tmA, fb, kb * kBK, tl.I * kBM + half, tl.idx);
+          // A and B are stored as their 256 x 256 blocks on and above the
+          // diagonal: an operand block below it is read as the transpose of
+          // the stored block (MN-major, two 64 x 64 boxes)
+          const int jb = kb * kBK / kBN;  // block column of this k block
+          // an MN-major half of A read transposed (128 columns = two 64-column
+          // atoms): one 4-D copy where the map exists, else two 3-D copies
+          auto load_t = [&](uint32_t dst, int col) {
+            if (C.t4) {
+              ptx::tma_load_4d_pair(dst, &C.tmT4, fb, 0, kb * kBK, col / 64, tl.idx);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 2; ++j)
+                ptx::tma_load_3d_pair(dst + j * (64 * kBK * 2), &C.tmT, fb, col + 64 * j, kb * kBK, tl.idx);
+            }
+          };
+          if (MODE == kPoly && SYM && jb < tl.I) {
+            load_t(sa, tl.I * kBM + half);
+          } else {
+            ptx::tma_load_3d_pair(sa, &C.tmA, fb, kb * kBK, tl.I * kBM + half, tl.idx);
+          }
           if (MODE == kUpdate) {
 #pragma unroll
             for (int j = 0; j < (kBN / 2) / 64; ++j)
               ptx::tma_load_3d_pair(sb + j * (64 * kBK * 2), &C.tmB, fb, tl.J * kBN + half + 64 * j, kb * kBK,
                                     tl.idx);
+          } else if (MODE == kPoly && SYM && jb < tl.J) {
+            load_t(sb, tl.J * kBN + half);
           } else {
             ptx::tma_load_3d_pair(sb, &C.tmB, fb, kb * kBK, tl.J * kBN + half, tl.idx);
           }
@@ -203,7 +240,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   } else if (warp == 1) {
     if (lane == 0 && rank == 0 && !P.inject_stall) {
       // ---------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = ptx::idesc_bf16(kBM, kBN, 0, MODE == kUpdate ? 1 : 0);
+      // instruction descriptors by operand major-ness (A, B): K-major, or
+      // MN-major for transposed reads of blocks below the diagonal
+      constexpr uint32_t idesc_kk = ptx::idesc_bf16(kBM, kBN, 0, 0);
+      constexpr uint32_t idesc_km = ptx::idesc_bf16(kBM, kBN, 0, 1);
+      constexpr uint32_t idesc_mk = ptx::idesc_bf16(kBM, kBN, 1, 0);
+      constexpr uint32_t idesc_mm = ptx::idesc_bf16(kBM, kBN, 1, 1);
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
@@ -234,11 +276,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           ptx::tc_fence_after();
           const uint32_t sa = ptx::smem_addr(smem + stage * kStageBytes);
           const uint32_t sb = sa + kStageA;
+          const int jb = kb * kBK / kBN;
+          const bool a_mn = MODE == kPoly && SYM && jb < tl.I;
+          const bool b_mn = MODE == kUpdate || (MODE == kPoly && SYM && jb < tl.J);
+          const uint32_t idesc = a_mn ? (b_mn ? idesc_mm : idesc_mk) : (b_mn ? idesc_km : idesc_kk);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
-            const uint64_t adesc = ptx::sdesc_sw128(sa + k * 32, 16, 1024);
-            const uint64_t bdesc = MODE == kUpdate ? ptx::sdesc_sw128(sb + k * 2048, 64 * kBK * 2, 1024)
-                                                   : ptx::sdesc_sw128(sb + k * 32, 16, 1024);
+            const uint64_t adesc = a_mn ? ptx::sdesc_sw128(sa + k * 2048, 64 * kBK * 2, 1024)
+                                        : ptx::sdesc_sw128(sa + k * 32, 16, 1024);
+            const uint64_t bdesc = b_mn ? ptx::sdesc_sw128(sb + k * 2048, 64 * kBK * 2, 1024)
+                                        : ptx::sdesc_sw128(sb + k * 32, 16, 1024);
             ptx::mma_bf16_pair(d, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
           }
           ptx::mma_commit_pair_mc(ptx::smem_addr(&empty[stage]), 0x3);
@@ -268,8 +315,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     // lane 0 stores as soon as the warp has written it (the first store
     // overlaps the second box) and reloads for the warp's next tile once the
     // store has read it, on the warp's own input barrier.  No barrier spans
-    // warps.  Gram and polynomial tiles above the diagonal also write their
-    // mirrored entries from registers, coalesced across the warp.
+    // warps.
     // The layout is TMA's 128-byte swizzle: boxes of 64 columns, rows of
     // 128 bytes, 16-byte piece j of row r at piece (j ^ (r % 8)).
     const int q = warp & 3;
@@ -326,7 +372,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       if (prof && elected) prof[kWpEpiTfull] += w4 - w3;
       ptx::tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN + colhalf * (kBN / 2);
-      uint32_t w[4][16];
+      uint32_t w[4][16];  // the rounded tile, kept for the mirrored writes
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t r[32];
@@ -347,6 +393,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         for (int jj = 0; jj < 4; ++jj) {
           const uint32_t addr = rowa + ((((j0 + jj) ^ (row_local & 7))) << 4);
           float v[8];
+          uint32_t wq[4];
           if (MODE == kGram) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(r[8 * jj + e]);
@@ -367,8 +414,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
             }
           }
 #pragma unroll
-          for (int e = 0; e < 4; ++e) w[ch][4 * jj + e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
-          ptx::sts128(addr, w[ch][4 * jj], w[ch][4 * jj + 1], w[ch][4 * jj + 2], w[ch][4 * jj + 3]);
+          for (int e = 0; e < 4; ++e) wq[e] = w[ch][4 * jj + e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
+          ptx::sts128(addr, wq[0], wq[1], wq[2], wq[3]);
         }
         if (ch == 3) {
           // accumulator drained: the MMA warp may reuse it
@@ -383,9 +430,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           if (lane == 0) store_box(C, tl, 2 * colhalf + (ch >> 1));
         }
       }
-      if (MODE != kUpdate && tl.I != tl.J) {
-        // mirrored entries (r, c) -> (c, r), straight from registers: a warp
-        // writes 32 adjacent r of one row c (64 contiguous bytes) per store
+      if ((MODE == kPoly || (MODE == kGram && !SYM)) && tl.I != tl.J) {
+        // B (and A of wide matrices) is stored whole: mirrored entries
+        // (r, c) -> (c, r) straight from registers, a warp writing 32
+        // adjacent r of one row c (64 contiguous bytes) per store
         const int rg = tl.I * kBM + rowoff + row_local;
         if (rg < C.m) {
           uint16_t* mcol = reinterpret_cast<uint16_t*>(C.out + tl.idx * C.out_mat_stride) + rg;
@@ -438,22 +486,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   }
 }
 
-template __global__ void ns_gemm_kernel<kGram>(const __grid_constant__ GemmParams P);
-template __global__ void ns_gemm_kernel<kPoly>(const __grid_constant__ GemmParams P);
-template __global__ void ns_gemm_kernel<kUpdate>(const __grid_constant__ GemmParams P);
+template __global__ void ns_gemm_kernel<kGram, 0>(const __grid_constant__ GemmParams P);
+template __global__ void ns_gemm_kernel<kGram, 1>(const __grid_constant__ GemmParams P);
+template __global__ void ns_gemm_kernel<kPoly, 0>(const __grid_constant__ GemmParams P);
+template __global__ void ns_gemm_kernel<kPoly, 1>(const __grid_constant__ GemmParams P);
+template __global__ void ns_gemm_kernel<kUpdate, 0>(const __grid_constant__ GemmParams P);
 
 // ------------------------------------------------------------------ launcher
 // Clusters of two CTAs (one pair per cluster), persistent: as many pairs as
 // can be resident at once, at most one per tile.
-cudaError_t launch_ns_gemm(int mode, const GemmParams& P, int num_sms, cudaStream_t stream) {
-  const void* fn = mode == kGram   ? reinterpret_cast<const void*>(&ns_gemm_kernel<kGram>)
-                   : mode == kPoly ? reinterpret_cast<const void*>(&ns_gemm_kernel<kPoly>)
-                                   : reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate>);
+cudaError_t launch_ns_gemm(int mode, int sym, const GemmParams& P, int num_sms, cudaStream_t stream) {
+  sym = mode == kUpdate ? 0 : (sym ? 1 : 0);
+  const void* fn =
+      mode == kGram ? (sym ? reinterpret_cast<const void*>(&ns_gemm_kernel<kGram, 1>)
+                           : reinterpret_cast<const void*>(&ns_gemm_kernel<kGram, 0>))
+      : mode == kPoly ? (sym ? reinterpret_cast<const void*>(&ns_gemm_kernel<kPoly, 1>)
+                             : reinterpret_cast<const void*>(&ns_gemm_kernel<kPoly, 0>))
+                      : reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate, 0>);
+  const int slot = mode * 2 + sym;
   const int smem = mode == kGram ? GemmShape<kGram>::smem : mode == kPoly ? GemmShape<kPoly>::smem
                                                                          : GemmShape<kUpdate>::smem;
-  static int max_pairs[3] = {0, 0, 0};
+  static int max_pairs[6] = {0, 0, 0, 0, 0, 0};
   cudaError_t e = cudaSuccess;
-  if (max_pairs[mode] <= 0) {
+  if (max_pairs[slot] <= 0) {
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
   }
@@ -470,14 +525,14 @@ cudaError_t launch_ns_gemm(int mode, const GemmParams& P, int num_sms, cudaStrea
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (max_pairs[mode] <= 0) {
+  if (max_pairs[slot] <= 0) {
     cfg.gridDim = dim3(num_sms);
     int n = 0;
     e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
     if (e != cudaSuccess) return e;
-    max_pairs[mode] = n > 0 ? n : 1;
+    max_pairs[slot] = n > 0 ? n : 1;
   }
-  int pairs = max_pairs[mode] < num_sms / 2 ? max_pairs[mode] : num_sms / 2;
+  int pairs = max_pairs[slot] < num_sms / 2 ? max_pairs[slot] : num_sms / 2;
   if (P.total_tiles < pairs) pairs = P.total_tiles;
   if (pairs <= 0) return cudaSuccess;
   cfg.gridDim = dim3(2 * pairs);

@@ -87,15 +87,19 @@ struct GemmClass {
                                 //            update: MN-major box 64 x 64)
   CUtensorMap tmAux;            // epilogue input tile (A or X_t), box 64 x 128
   CUtensorMap tmOut;            // output tile, box 64 x 128
-  CUtensorMap tmOutT;           // unused (kept for layout)
-  __nv_bfloat16* out;           // output region (mirrored writes of Gram/poly)
+  CUtensorMap tmT;              // poly: A's stored blocks read transposed
+                                //   (MN-major, box 64 x 64)
+  CUtensorMap tmT4;             // the same as 4-D (64 columns, rows, 64-column
+                                //   chunk, matrix): both atoms in one copy
+  __nv_bfloat16* out;           // poly: B, for the mirrored writes
   long long out_mat_stride;     // elements between matrices of out
   int ld_out;
   int m, n, count, K;
   int tiles_m, tiles_n, tiles_per_mat;
   int tile_begin;
   int mat_begin;
-  int pad[3];
+  int t4;                       // 1: tmT4 is valid (width a multiple of 64)
+  int pad[2];
 };
 
 struct GemmParams {
@@ -158,6 +162,13 @@ constexpr int kGemmSmem = kStages * kStageBytes + kStageOut + 1024 /*align*/ + 2
 // staging holds one 64 x 32 box per warp (32 KB, reused for the warp's second
 // box once the first has been stored) and the space freed is a sixth operand
 // stage; the polynomial and update tiles stage the input next to the output.
+// Gram / poly: the largest m for which A is stored as its blocks on and above
+// the diagonal only, the polynomial reading the others transposed.  Transposed
+// reads walk 64 rows per K block; for wider matrices their lost locality costs
+// the polynomial more than the Gram's mirrored writes cost (measured on
+// 768-, 1024-, 1600- and 4096-wide banks).
+constexpr int kSymUpperMaxM = 768;
+
 template <int MODE>
 struct GemmShape {
   static constexpr int stages = MODE == kGram ? kStages + 1 : kStages;

@@ -45,6 +45,23 @@ def ws_view(ws, offset, rows, cols, ld, batch=1, index=0):
     return t.float().cpu().numpy().astype(np.float64)
 
 
+def sym_from_upper_blocks(M, block=256):
+    """The full symmetric matrix from its stored blocks on and above the
+    diagonal (blocks below the diagonal are not written by the kernels)."""
+    F = M.copy()
+    m = M.shape[0]
+    for i0 in range(0, m, block):
+        for j0 in range(0, i0, block):
+            F[i0:i0 + block, j0:j0 + block] = M[j0:j0 + block, i0:i0 + block].T
+    return F
+
+
+def diagonal_blocks_symmetric(M, block=256):
+    m = M.shape[0]
+    return all(np.array_equal(M[i:i + block, i:i + block], M[i:i + block, i:i + block].T)
+               for i in range(0, m, block))
+
+
 def to_dev(a, dtype=torch.float32, device="cuda"):
     return torch.from_numpy(np.ascontiguousarray(a)).to(device=device).to(dtype)
 
