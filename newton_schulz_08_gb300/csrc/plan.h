@@ -156,7 +156,6 @@ constexpr int kStageA = (kBM / 2) * kBK * 2;  // 16 KB
 constexpr int kStageB = (kBN / 2) * kBK * 2;  // 16 KB
 constexpr int kStageBytes = kStageA + kStageB;
 constexpr int kStageOut = (kBM / 2) * kBN * 2;  // 64 KB epilogue staging
-constexpr int kGemmSmem = kStages * kStageBytes + kStageOut + 1024 /*align*/ + 256 /*barriers*/;
 
 // Shared-memory shape per phase.  A Gram tile has no epilogue input, so its
 // staging holds one 64 x 32 box per warp (32 KB, reused for the warp's second
