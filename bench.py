@@ -246,8 +246,10 @@ def run_reference(args, rank, world):
         }
         print(json.dumps(line), flush=True)
         return
-    # size each step so the whole run stays within about two minutes
-    n0, t0 = oracle_sample(shapes, 0.0, min_mats=1)
+    # size each step so the whole run stays within about two minutes (the
+    # cost per matrix from one pass over the bank's first six, which cover
+    # every shape of a layer)
+    n0, t0 = oracle_sample(shapes, 0.0, min_mats=min(6, len(shapes)))
     per_mat = t0 / n0
     per_step_budget = max(per_mat, 120.0 / max(1, args.steps + args.warmup))
     mats_per_step = max(1, int(per_step_budget / per_mat))
