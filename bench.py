@@ -89,6 +89,27 @@ def ns_flops(shapes, steps=NS_STEPS):
     return {k: v * steps for k, v in f.items()}
 
 
+def ns_flops_issued(shapes, steps=NS_STEPS):
+    """FLOPs the tensor cores execute for one step over the bank: whole
+    256 x 256 tiles (Gram / poly: the tiles on and above the diagonal),
+    K padded to 64."""
+    f = {"gram": 0.0, "poly": 0.0, "update": 0.0}
+    t, kb = 256, 64
+    for r, c in shapes:
+        m, n = min(r, c), max(r, c)
+        tm, tn = -(-m // t), -(-n // t)
+        upper = tm * (tm + 1) // 2
+        f["gram"] += 2.0 * upper * t * t * (-(-n // kb) * kb)
+        f["poly"] += 2.0 * upper * t * t * (-(-m // kb) * kb)
+        f["update"] += 2.0 * tm * tn * t * t * (-(-m // kb) * kb)
+    return {k: v * steps for k, v in f.items()}
+
+
+def ns_flops_dense(shapes, steps=NS_STEPS):
+    """Dense-equivalent FLOPs (X X^T, A A and B X as plain GEMMs): 4 m^2 n + 2 m^3."""
+    return steps * sum(4.0 * min(r, c) ** 2 * max(r, c) + 2.0 * min(r, c) ** 3 for r, c in shapes)
+
+
 def hbm_bytes(shapes, gbytes, ns5_only=False):
     """Algorithmic bytes of the elementwise passes for one step over the bank."""
     e = float(sum(r * c for r, c in shapes))
@@ -552,10 +573,12 @@ def main():
         if kind in flops:
             work = flops[kind] / per_step  # per launch
             ach = work / (avg * 1e-3) / 1e12
+            issued = ns_flops_issued(shapes)[kind] / per_step / (avg * 1e-3) / 1e12
             kern[kind] = {"avg_ms": avg, "launches_per_step": per_step, "share": None,
                           "achieved": ach, "unit": "TFLOP/s", "bound": "tensor",
                           "peak": peaks["bf16_tflops"], "frac": ach / peaks["bf16_tflops"],
-                          "work_per_launch": work}
+                          "work_per_launch": work, "issued_tflops": issued,
+                          "issued_frac": issued / peaks["bf16_tflops"]}
         else:
             work = gbytes[kind] / per_step
             ach = work / (avg * 1e-3) / 1e9
@@ -589,6 +612,8 @@ def main():
                                    "(no data exchanged)" if world > 1 else "1 GPU")},
         "ns5_tflops": total_flops / (ms * 1e-3) / 1e12,
         "ns5_tflops_note": "algorithmic NS FLOPs of the whole step / step time",
+        "ns5_tflops_issued": sum(ns_flops_issued(shapes).values()) / (ms * 1e-3) / 1e12,
+        "ns5_tflops_dense_equivalent": ns_flops_dense(shapes) / (ms * 1e-3) / 1e12,
         "update_gbs": (gbytes["momentum_cast"] + gbytes["apply"]) / (ms * 1e-3) / 1e9,
         "roofline": {"kernel": dom, "bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"],
                      "unit": d["unit"], "frac": d["frac"], "traffic": traffic,
