@@ -326,3 +326,27 @@ def test_cuda_graph_capture_replays_the_step():
     check_status(ws)
     for a, b in zip(P + B, want):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("steps", [0, 1, 2, 7])
+def test_muon_step_any_step_count(steps):
+    """The final X sits in ping-pong buffer (steps % 2); 0 steps applies X0."""
+    shapes = [(256, 256), (300, 100), (100, 300)]
+    lr, mu = 0.02, 0.95
+    ps, gs, bs, P, Bn = run_step(shapes, True, steps, torch.bfloat16, seed=31, lr=lr, mu=mu)
+    for i in range(len(shapes)):
+        _, new_buf, O = oracle.muon_step(ps[i], gs[i], bs[i], lr, mu, True, steps, "bf16")
+        assert rel(Bn[i], new_buf) <= TOL_BUF_REL
+        O_gpu = (ps[i].astype(np.float64) - P[i].astype(np.float64)) / lr
+        assert rel(O_gpu, O) <= TOL_REL_BF16, (steps, i)
+        assert np.abs(O_gpu - O).max() <= TOL_MAXABS_BF16
+
+
+def test_zero_lr_and_zero_momentum():
+    """lr = 0 leaves the parameters bit for bit; momentum 0 makes the buffer
+    the gradient (fp32 value of the bf16 gradient)."""
+    shapes = [(256, 256), (300, 100)]
+    ps, gs, bs, P, Bn = run_step(shapes, True, 5, torch.bfloat16, seed=32, lr=0.0, mu=0.0)
+    for i in range(len(shapes)):
+        assert np.array_equal(P[i], ps[i])
+        assert np.array_equal(Bn[i], gs[i])
