@@ -328,6 +328,15 @@ def test_cuda_graph_capture_replays_the_step():
         assert torch.equal(a, b)
 
 
+# The bf16 bound holds for up to five steps.  Two bf16 evaluations that differ
+# only in fp32 accumulation order drift apart with every further step: an
+# emulation of fp32 accumulation on these inputs is 6.7e-3 from the bf16
+# oracle after 5 steps and 1.18e-2 after 7 (256 x 256), so 7 steps get twice
+# the bound, and the fp64 bound, which the bf16 oracle itself meets with room
+# (1.6-1.8e-2 after 7 steps), as well.
+STEP_COUNT_TOL_BF16 = {0: TOL_REL_BF16, 1: TOL_REL_BF16, 2: TOL_REL_BF16, 7: 2 * TOL_REL_BF16}
+
+
 @pytest.mark.parametrize("steps", [0, 1, 2, 7])
 def test_muon_step_any_step_count(steps):
     """The final X sits in ping-pong buffer (steps % 2); 0 steps applies X0."""
@@ -336,9 +345,11 @@ def test_muon_step_any_step_count(steps):
     ps, gs, bs, P, Bn = run_step(shapes, True, steps, torch.bfloat16, seed=31, lr=lr, mu=mu)
     for i in range(len(shapes)):
         _, new_buf, O = oracle.muon_step(ps[i], gs[i], bs[i], lr, mu, True, steps, "bf16")
+        _, _, O64 = oracle.muon_step(ps[i], gs[i], bs[i], lr, mu, True, steps, "fp64")
         assert rel(Bn[i], new_buf) <= TOL_BUF_REL
         O_gpu = (ps[i].astype(np.float64) - P[i].astype(np.float64)) / lr
-        assert rel(O_gpu, O) <= TOL_REL_BF16, (steps, i)
+        assert rel(O_gpu, O) <= STEP_COUNT_TOL_BF16[steps], (steps, i, rel(O_gpu, O))
+        assert rel(O_gpu, O64) <= TOL_REL_FP64, (steps, i, rel(O_gpu, O64))
         assert np.abs(O_gpu - O).max() <= TOL_MAXABS_BF16
 
 
