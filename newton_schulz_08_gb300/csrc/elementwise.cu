@@ -17,8 +17,9 @@
 // normalise: X0 = bf16(Xraw * (1 / (sqrt(sum of the matrix's partials) +
 //   1e-7))), in place; the partials are summed in a fixed order by every
 //   block.
-// apply: after the last step, p <- p - lr * O (or O written), O = X in the
-//   stored orientation.
+// apply: after the last step, O = X in the stored orientation written
+//   (Newton-Schulz alone), or p <- p - lr * O for a Muon step with no
+//   iteration (otherwise the last update applies it).
 #include "plan.h"
 
 namespace muon {
@@ -446,8 +447,9 @@ __global__ void __launch_bounds__(kEwThreads, 5) normalise_kernel(const __grid_c
   }
 }
 
-// apply: O = X_final in the matrix's stored orientation; the Muon step does
-// p <- p - lr * O (fp32 FMA), Newton-Schulz alone writes O (bf16).  One
+// apply: O = X_final in the matrix's stored orientation; Newton-Schulz alone
+// writes O (bf16), a Muon step with no iteration does p <- p - lr * O (fp32
+// FMA; with iterations the last update does it).  One
 // 64 x 64 tile of X per block.  Tall matrices (O = X^T) go through a shared
 // tile so that both the reads of X and the accesses to p / O are contiguous
 // across a warp.

@@ -8,9 +8,11 @@
 //                      transpose of tall matrices, partial norms
 //   normalise          1 launch: X0 = bf16(Xraw / (||Xraw||_F + 1e-7))
 //   ns_steps x { Gram, Poly, Update }   1 persistent launch each for the
-//                      whole bank (per group of <= 8 shape classes)
-//   apply              1 launch: p <- p - lr O (or O written), O = final X
-//                      transposed back for tall matrices
+//                      whole bank (per group of <= 8 shape classes); in the
+//                      Muon step the last Update also applies p <- p - lr O
+//   apply              Newton-Schulz alone (or a step with no iteration):
+//                      1 launch, O = final X transposed back for tall
+//                      matrices written (or p <- p - lr O)
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -456,6 +458,10 @@ muon_status_t run(const std::vector<JobMat>& mats, const Plan& P, float lr, floa
         gp.wait_budget = budget;
         gp.inject_stall = stall;
         gp.wait_profile = reinterpret_cast<long long*>(g_wait_profile.load());
+        // the Muon step's last update applies p -= lr X' itself
+        gp.table = table;
+        gp.lr = lr;
+        gp.apply = mode == kUpdate && final_mode == kFinalParam && t == ns_steps - 1;
         EventPair ev;
         const bool rec = ev_begin(ev, 2 + mode, stream);
         if (launch_ns_gemm(mode, sym, gp, sms, stream) != cudaSuccess) return MUON_ERR_CUDA;
@@ -465,7 +471,9 @@ muon_status_t run(const std::vector<JobMat>& mats, const Plan& P, float lr, floa
     }
   }
 
-  // O = final X (transposed back); p <- p - lr O, or O written
+  // O = final X (transposed back) written, or, with no Newton-Schulz step,
+  // p <- p - lr O (the last update has applied it otherwise)
+  if (final_mode == kFinalParam && ns_steps > 0) return MUON_OK;
   const int fin = ns_steps & 1;
   for (size_t c0 = 0; c0 < P.cls.size(); c0 += kMaxClasses) {
     ApplyParams ap;

@@ -22,8 +22,9 @@
 //             writes the mirrored entries, so B is stored whole.
 //   kUpdate : X' = a X + B X.     All tiles of the m x n result; B is the
 //             K-major A operand, X the MN-major B operand.  The epilogue
-//             reads X's tile and fuses a X + (.).  (The parameter update
-//             after the last step is a separate coalesced pass, apply_kernel.)
+//             reads X's tile and fuses a X + (.).  In the last step of the
+//             Muon step it applies p <- p - lr X' (fp32, in p's own layout)
+//             instead of storing X'.
 //
 // Kernel structure: clusters of two CTAs on neighbouring SMs; each pair
 // computes 256 x 256 output tiles with tcgen05.mma.cta_group::2 (M = 256 over
@@ -345,6 +346,54 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
                         tl.I * kBM + rowoff + q * kEpiRows, tl.idx);
       ptx::bulk_commit();
     };
+    // p <- p - lr X' for this warp's 32 rows of box bx (64 columns of X'),
+    // p stored like X (R = m rows of n): the rounded X' is read back from the
+    // staging tile, half a warp per row and 4 columns (16 bytes of p) per
+    // lane, all 16 of a lane's loads in flight before its stores
+    auto apply_box = [&](const GemmClass& C, const Tile& tl, float* pm, int bx) {
+      __syncwarp();
+      const uint32_t box = stg_a + bx * ((kBM / 2) * 128);
+      const int cl = (lane & 15) * 4;
+      const int cg = tl.J * kBN + 64 * bx + cl;
+      const bool vec = (C.n & 3) == 0;  // rows 16-byte aligned
+      {
+        float pv[16][4];
+        uint32_t xv[16][2];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int rl = q * kEpiRows + 2 * k + (lane >> 4);
+          const int r = tl.I * kBM + rowoff + rl;
+          ptx::lds64(box + rl * 128 + (((cl >> 3) ^ (rl & 7)) << 4) + (cl & 7) * 2, xv[k][0], xv[k][1]);
+          const float* pp = pm + static_cast<long long>(r) * C.n + cg;
+          if (r < C.m && vec && cg < C.n) {
+            const float4 f = *reinterpret_cast<const float4*>(pp);
+            pv[k][0] = f.x;
+            pv[k][1] = f.y;
+            pv[k][2] = f.z;
+            pv[k][3] = f.w;
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) pv[k][e] = (r < C.m && cg + e < C.n) ? pp[e] : 0.0f;
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int rl = q * kEpiRows + 2 * k + (lane >> 4);
+          const int r = tl.I * kBM + rowoff + rl;
+          float o[4] = {word_lo(xv[k][0]), word_hi(xv[k][0]), word_lo(xv[k][1]), word_hi(xv[k][1])};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[e] = fmaf(-P.lr, o[e], pv[k][e]);
+          float* pp = pm + static_cast<long long>(r) * C.n + cg;
+          if (r < C.m && vec && cg < C.n) {
+            *reinterpret_cast<float4*>(pp) = make_float4(o[0], o[1], o[2], o[3]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (r < C.m && cg + e < C.n) pp[e] = o[e];
+          }
+        }
+      }
+    };
     if (MODE != kGram && lane == 0 && pair < P.total_tiles) load_aux(pair);
     uint32_t aux_phase = 0;
     bool ok = true;
@@ -354,6 +403,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       const GemmClass& C = P.cls[tl.cls];
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
+      // the Muon step's last update: p <- p - lr X' instead of storing X'
+      const bool fuse = MODE == kUpdate && P.apply;
+      float* pm = nullptr;
+      bool ptall = false;
+      if (fuse) {
+        const MatInfo& mi = P.table[C.mat_begin + tl.idx];
+        pm = static_cast<float*>(mi.out);
+        ptall = mi.tall != 0;
+      }
       if (MODE != kGram) {
         if (!ptx::mbar_wait(ptx::smem_addr(my_aux), aux_phase, budget, abort)) {
           raise_timeout(P, abort);
@@ -375,11 +433,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       uint32_t w[4][16];  // the rounded tile, kept for the mirrored writes
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
+        const int c0 = colhalf * (kBN / 2) + ch * 32;  // column within the tile
+        // tall p (Muon step's last update): p = X'^T, n rows of m.  For X
+        // column c the warp's 32 rows are 32 consecutive floats of p's row c,
+        // one coalesced 128-byte access; the chunk's loads are issued before
+        // its accumulator columns are read
+        float pv[32];
+        float* pc = nullptr;
+        const int rt = tl.I * kBM + rowoff + row_local;
+        const int ct = tl.J * kBN + c0;
+        if (MODE == kUpdate && fuse && ptall) {
+          pc = pm + static_cast<long long>(ct) * C.m + rt;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            pv[j] = (rt < C.m && ct + j < C.n) ? pc[static_cast<long long>(j) * C.m] : 0.0f;
+        }
         uint32_t r[32];
         __syncwarp();
         ptx::tmem_ld32(tb + ch * 32, r);
         ptx::tmem_ld_wait();
-        const int c0 = colhalf * (kBN / 2) + ch * 32;  // column within the tile
         // staging box: the tile's 64-column box, or (Gram) the warp's one box
         const int sbx = MODE == kGram ? colhalf : (c0 >> 6);
         const uint32_t rowa = stg_a + sbx * ((kBM / 2) * 128) + row_local * 128;
@@ -389,6 +461,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           __syncwarp();
         }
         const int j0 = (c0 & 63) >> 3;
+        uint32_t ow[16];  // this chunk's 32 rounded values (pairs)
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
           const uint32_t addr = rowa + ((((j0 + jj) ^ (row_local & 7))) << 4);
@@ -414,8 +487,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
             }
           }
 #pragma unroll
-          for (int e = 0; e < 4; ++e) wq[e] = w[ch][4 * jj + e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
-          ptx::sts128(addr, wq[0], wq[1], wq[2], wq[3]);
+          for (int e = 0; e < 4; ++e) {
+            wq[e] = ow[4 * jj + e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
+            if (MODE != kUpdate) w[ch][4 * jj + e] = wq[e];
+          }
+          if (!(fuse && ptall)) ptx::sts128(addr, wq[0], wq[1], wq[2], wq[3]);
+        }
+        if (MODE == kUpdate && fuse && ptall) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float o = (j & 1) ? word_hi(ow[j >> 1]) : word_lo(ow[j >> 1]);
+            if (rt < C.m && ct + j < C.n) pc[static_cast<long long>(j) * C.m] = fmaf(-P.lr, o, pv[j]);
+          }
         }
         if (ch == 3) {
           // accumulator drained: the MMA warp may reuse it
@@ -425,9 +508,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         }
         if (ch & 1) {
           // this warp's rows of box 2*colhalf + ch/2 are written: store them
-          ptx::fence_async_smem();
-          __syncwarp();
-          if (lane == 0) store_box(C, tl, 2 * colhalf + (ch >> 1));
+          // (or apply them to p)
+          if (MODE == kUpdate && fuse) {
+            if (!ptall) apply_box(C, tl, pm, 2 * colhalf + (ch >> 1));
+          } else {
+            ptx::fence_async_smem();
+            __syncwarp();
+            if (lane == 0) store_box(C, tl, 2 * colhalf + (ch >> 1));
+          }
         }
       }
       if ((MODE == kPoly || (MODE == kGram && !SYM)) && tl.I != tl.J) {
@@ -448,6 +536,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
             }
           }
         }
+      }
+      if (MODE == kUpdate && fuse) {
+        // the staging rows were read with ordinary loads: order those reads
+        // before the copy of the next input tile overwrites them
+        ptx::fence_async_smem();
+        __syncwarp();
       }
       if (lane == 0) {
         ptx::bulk_wait_read0();  // this warp's rows are free again

@@ -112,6 +112,10 @@ struct GemmParams {
   int inject_stall;             // test hook: MMA warp issues nothing
   int pad;
   long long* wait_profile;      // diagnostics: kWaitCounters per CTA, or null
+  const MatInfo* table;         // update of the Muon step's last iteration:
+  float lr;                     //   the matrices' parameters and the rate
+  int apply;                    // 1: the epilogue applies p <- p - lr X' (fp32,
+                                //   in p's own layout) instead of storing X'
 };
 
 // diagnostics counters per CTA (clock64 cycles unless noted)

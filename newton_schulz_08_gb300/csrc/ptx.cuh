@@ -257,6 +257,10 @@ __device__ __forceinline__ void lds128(uint32_t addr, uint32_t& a, uint32_t& b, 
                : "memory");
 }
 
+__device__ __forceinline__ void lds64(uint32_t addr, uint32_t& a, uint32_t& b) {
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(addr) : "memory");
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle.
 //   K-major tiles: rows of 128 B (64 bf16 along K), 8-row groups 1024 B
 //     apart (SBO); LBO unused.

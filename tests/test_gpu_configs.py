@@ -61,7 +61,6 @@ def test_single_128x512():
     p, g, b = inputs.single()
     R, C = cfg["shape"]
     P, Bd, Gd = to_dev(p), to_dev(b), to_dev(g)
-    lay = muon.ns5_workspace_layout(1, R, C)
     ws = muon.new_workspace(muon.muon_workspace_size([(R, C)]))
     muon.muon_step([P], [Gd], [Bd], lr=cfg["lr"], momentum=cfg["momentum"], nesterov=True,
                    ns_steps=cfg["ns_steps"], workspace=ws)
@@ -69,16 +68,12 @@ def test_single_128x512():
     new_p, new_buf, O = oracle.muon_step(p, g, b, LR, MU, True, 5, "bf16")
     # (i) momentum buffer
     assert rel(Bd.cpu().numpy(), new_buf) <= TOL_BUF_REL
-    # (ii) the fused update given the GPU's own O (final X kept in the workspace)
-    X5 = ws[lay["x_offset"][1]:lay["x_offset"][1] + 2 * R * lay["ldx"]].view(torch.bfloat16)
-    O_gpu = X5.view(R, lay["ldx"])[:, :C].float().cpu().numpy()
-    want_p = (p - np.float32(LR) * O_gpu).astype(np.float32)
-    assert rel(P.cpu().numpy(), want_p) <= 1e-5
-    # (iii) O against the oracles
+    # (ii) O, recovered from the parameter change, against the oracles (the
+    # update itself is checked bit for bit in test_gpu_kernels)
     O_from_p = (p.astype(np.float64) - P.cpu().numpy()) / LR
     _, u = oracle.momentum_update(g, b, MU, True, "bf16")
     check_O(O_from_p, u, "single")
-    assert rel(O_gpu, O) <= TOL_REL_BF16
+    assert rel(O_from_p, O) <= TOL_REL_BF16
 
 
 # ---------------------------------------------------------------- gpt2 bank

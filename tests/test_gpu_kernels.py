@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle
-from newton_schulz_08_gb300 import muon
+from newton_schulz_08_gb300 import inputs, muon
 from tests.gpu_helpers import (TOL_BUF_REL, TOL_MAXABS_BF16, TOL_REL_BF16, TOL_REL_FP64,
                                assert_bf16_close, bf16_np, check_status, diagonal_blocks_symmetric, rel,
                                sym_from_upper_blocks, to_dev, ws_view)
@@ -200,26 +200,6 @@ def test_extreme_aspect_ratios(shape):
     check_bank_against_oracle([shape], ps, gs, bs, P, Bn)
 
 
-def test_param_update_is_exact_given_gpu_O():
-    """p_new = p - lr * O_gpu in fp32, O_gpu read from the workspace."""
-    R, C = 300, 100
-    rng = np.random.default_rng(6)
-    p = (rng.standard_normal((R, C)) * 0.02).astype(np.float32)
-    g = rng.standard_normal((R, C)).astype(np.float32)
-    b = np.zeros((R, C), np.float32)
-    P, Gd, Bd = to_dev(p), to_dev(g), to_dev(b)
-    lay = muon.ns5_workspace_layout(1, R, C)
-    ws = muon.new_workspace(muon.muon_workspace_size([(R, C)]))
-    muon.muon_step([P], [Gd], [Bd], lr=0.02, momentum=0.95, ns_steps=5, workspace=ws)
-    check_status(ws)
-    X5 = ws_view(ws, lay["x_offset"][1], lay["m"], lay["n"], lay["ldx"])  # 5 steps end in buffer 1
-    O = X5.T  # tall
-    want = (p - np.float32(0.02) * O.astype(np.float32)).astype(np.float32)
-    got = P.cpu().numpy()
-    assert np.abs(got - want).max() <= 1e-5 * np.abs(want).max()
-    assert rel(got, want) <= 1e-5
-
-
 def test_zero_matrix_leaves_param():
     p = np.random.default_rng(7).standard_normal((128, 256)).astype(np.float32)
     P = to_dev(p)
@@ -351,6 +331,35 @@ def test_muon_step_any_step_count(steps):
         assert rel(O_gpu, O) <= STEP_COUNT_TOL_BF16[steps], (steps, i, rel(O_gpu, O))
         assert rel(O_gpu, O64) <= TOL_REL_FP64, (steps, i, rel(O_gpu, O64))
         assert np.abs(O_gpu - O).max() <= TOL_MAXABS_BF16
+
+
+@pytest.mark.parametrize("shape", [(256, 256), (300, 100), (100, 300), (520, 1030), (1030, 520), (130, 258),
+                                   (77, 45), (45, 77), (768, 3072), (3072, 768)])
+def test_parameter_update_is_one_fma_per_entry(shape):
+    """The last update applies p <- p - lr O in its epilogue, O the
+    bf16-rounded final X.  With momentum 0 the step's X is the gradient
+    itself, so ns5 of the same gradient (given as float32, which takes the
+    same cast-and-norm loop) yields the step's O bit for bit, and every
+    parameter must equal fl32(p - lr O): one fused multiply-add (lr O is
+    exact in float64, and so is the difference here).  Wide, tall and ragged
+    shapes: the tall path writes p's rows straight from registers, the wide
+    path sweeps the staged rows, and n % 4 != 0 takes the scalar path."""
+    lr = np.float32(0.02)
+    p = inputs.param(shape, 40)
+    g = oracle.round_to_bf16(inputs.grad(shape, 40)).astype(np.float32)
+    dev = torch.device("cuda")
+    P = torch.from_numpy(p).to(dev)
+    G = torch.from_numpy(g).to(dev).to(torch.bfloat16)
+    B = torch.zeros_like(P)
+    ws = muon.muon_step([P], [G], [B], lr=float(lr), momentum=0.0, nesterov=True, ns_steps=5)
+    O = muon.ns5(G.float(), 5)
+    torch.cuda.synchronize()
+    check_status(ws)
+    O = O.float().cpu().numpy().astype(np.float64)
+    want = (p.astype(np.float64) - np.float64(lr) * O).astype(np.float32)
+    got = P.cpu().numpy()
+    same = got.view(np.uint32) == want.view(np.uint32)
+    assert same.all(), (int((~same).sum()), got.size)
 
 
 def test_zero_lr_and_zero_momentum():
