@@ -117,9 +117,12 @@ def hbm_bytes(shapes, gbytes, ns5_only=False):
         return {"momentum_cast": e * (gbytes + 2),       # G r, Xraw w
                 "normalise": e * 4,                      # Xraw r, X0 w
                 "apply": e * (2 + 2)}                    # X r, O w
+    b_bytes = float(sum(2 * min(r, c) ** 2 for r, c in shapes))
     return {"momentum_cast": e * (gbytes + 4 + 4 + 2),  # g, buf r/w, Xraw
             "normalise": e * 4,                          # Xraw r, X0 w
-            "apply": e * (2 + 4 + 4)}                    # X r, p r/w
+            "apply": e * (2 + 4 + 4),                    # X r, p r/w
+            # the Muon step's last update: X and B read, p read and written
+            "update_apply": e * (2 + 4 + 4) + b_bytes}
 
 
 def load_peaks():
@@ -564,16 +567,22 @@ def main():
     peaks, peak_src = load_peaks()
     flops = ns_flops(shapes)
     gbytes = hbm_bytes(shapes, gbytes, ns5_only)
+    # per kind: the work of the launches timed under it (the last of the
+    # NS_STEPS updates is timed as update_apply when the step applies p there)
+    kflops, kissued = dict(flops), ns_flops_issued(shapes)
+    if ktimes.get("update_apply", (0, 0))[1]:
+        for f in (kflops, kissued):
+            f["update"] *= (NS_STEPS - 1) / NS_STEPS
     kern = {}
     for kind, (tot_ms, cnt) in ktimes.items():
         if cnt == 0:
             continue
         avg = tot_ms / cnt
         per_step = cnt / args.steps
-        if kind in flops:
-            work = flops[kind] / per_step  # per launch
+        if kind in kflops:
+            work = kflops[kind] / per_step  # per launch
             ach = work / (avg * 1e-3) / 1e12
-            issued = ns_flops_issued(shapes)[kind] / per_step / (avg * 1e-3) / 1e12
+            issued = kissued[kind] / per_step / (avg * 1e-3) / 1e12
             kern[kind] = {"avg_ms": avg, "launches_per_step": per_step, "share": None,
                           "achieved": ach, "unit": "TFLOP/s", "bound": "tensor",
                           "peak": peaks["bf16_tflops"], "frac": ach / peaks["bf16_tflops"],

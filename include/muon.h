@@ -161,9 +161,10 @@ int muon_set_debug(const char* key, long long value);
  * "record_kernel_events") and returns, per kernel kind, the summed
  * milliseconds and the launch count: kind 0 momentum_cast, 1 normalise,
  * 2 Gram (A = X X^T), 3 polynomial (B = b A + c A A), 4 update
- * (X = a X + B X; in muon_step's last iteration it also applies
- * p <- p - lr O), 5 apply (O written by ns5, or p <- p - lr O for a step
- * with no iteration).  ms and launches are host arrays of n_kinds entries.
+ * (X = a X + B X), 5 apply (O written by ns5, or p <- p - lr O for a step
+ * with no iteration), 6 muon_step's last update (X = a X + B X with
+ * p <- p - lr O applied in place of storing X).  ms and launches are host
+ * arrays of n_kinds entries; kinds at or above n_kinds are not reported.
  * Returns 0, or -1 on a bad argument or a failed event query. */
 int muon_kernel_times(double* ms, int* launches, int n_kinds);
 

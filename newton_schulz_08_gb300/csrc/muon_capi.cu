@@ -50,7 +50,8 @@ std::atomic<int> g_record_events{0};
 std::atomic<long long> g_wait_profile{0};  // device address of the counters, 0: off
 
 // Optional CUDA-event brackets around every launch (diagnostics).
-// kinds: 0 momentum_cast, 1 normalise, 2 gram, 3 poly, 4 update, 5 apply
+// kinds: 0 momentum_cast, 1 normalise, 2 gram, 3 poly, 4 update, 5 apply,
+// 6 the Muon step's last update (p <- p - lr O applied in its epilogue)
 struct EventPair {
   cudaEvent_t start, stop;
   int kind;
@@ -463,7 +464,7 @@ muon_status_t run(const std::vector<JobMat>& mats, const Plan& P, float lr, floa
         gp.lr = lr;
         gp.apply = mode == kUpdate && final_mode == kFinalParam && t == ns_steps - 1;
         EventPair ev;
-        const bool rec = ev_begin(ev, 2 + mode, stream);
+        const bool rec = ev_begin(ev, gp.apply ? 6 : 2 + mode, stream);
         if (launch_ns_gemm(mode, sym, gp, sms, stream) != cudaSuccess) return MUON_ERR_CUDA;
         ev_end(ev, rec, stream);
        }

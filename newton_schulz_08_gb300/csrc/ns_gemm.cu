@@ -112,7 +112,10 @@ __device__ __forceinline__ float word_hi(uint32_t w) { return __uint_as_float(w 
 // no mirrored entries and the polynomial reads the blocks below the diagonal
 // transposed.  A compile-time choice, so that the other classes run code
 // without any of it.
-template <int MODE, int SYM>
+// APPLY (update only): the Muon step's last update, which applies
+// p <- p - lr X' instead of storing X'; also compile-time, so that the other
+// updates run without its registers.
+template <int MODE, int SYM, int APPLY>
 __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -404,7 +407,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
       // the Muon step's last update: p <- p - lr X' instead of storing X'
-      const bool fuse = MODE == kUpdate && P.apply;
+      constexpr bool fuse = MODE == kUpdate && APPLY;
       float* pm = nullptr;
       bool ptall = false;
       if (fuse) {
@@ -580,24 +583,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   }
 }
 
-template __global__ void ns_gemm_kernel<kGram, 0>(const __grid_constant__ GemmParams P);
-template __global__ void ns_gemm_kernel<kGram, 1>(const __grid_constant__ GemmParams P);
-template __global__ void ns_gemm_kernel<kPoly, 0>(const __grid_constant__ GemmParams P);
-template __global__ void ns_gemm_kernel<kPoly, 1>(const __grid_constant__ GemmParams P);
-template __global__ void ns_gemm_kernel<kUpdate, 0>(const __grid_constant__ GemmParams P);
+template __global__ void ns_gemm_kernel<kGram, 0, 0>(const __grid_constant__ GemmParams P);
+template __global__ void ns_gemm_kernel<kGram, 1, 0>(const __grid_constant__ GemmParams P);
+template __global__ void ns_gemm_kernel<kPoly, 0, 0>(const __grid_constant__ GemmParams P);
+template __global__ void ns_gemm_kernel<kPoly, 1, 0>(const __grid_constant__ GemmParams P);
+template __global__ void ns_gemm_kernel<kUpdate, 0, 0>(const __grid_constant__ GemmParams P);
+template __global__ void ns_gemm_kernel<kUpdate, 0, 1>(const __grid_constant__ GemmParams P);
 
 // ------------------------------------------------------------------ launcher
 // Clusters of two CTAs (one pair per cluster), persistent: as many pairs as
 // can be resident at once, at most one per tile.
 cudaError_t launch_ns_gemm(int mode, int sym, const GemmParams& P, int num_sms, cudaStream_t stream) {
-  sym = mode == kUpdate ? 0 : (sym ? 1 : 0);
+  // Gram / polynomial: 1 = A stored block-upper; update: 1 = with the
+  // parameter update
+  const int variant = mode == kUpdate ? (P.apply ? 1 : 0) : (sym ? 1 : 0);
   const void* fn =
-      mode == kGram ? (sym ? reinterpret_cast<const void*>(&ns_gemm_kernel<kGram, 1>)
-                           : reinterpret_cast<const void*>(&ns_gemm_kernel<kGram, 0>))
-      : mode == kPoly ? (sym ? reinterpret_cast<const void*>(&ns_gemm_kernel<kPoly, 1>)
-                             : reinterpret_cast<const void*>(&ns_gemm_kernel<kPoly, 0>))
-                      : reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate, 0>);
-  const int slot = mode * 2 + sym;
+      mode == kGram ? (variant ? reinterpret_cast<const void*>(&ns_gemm_kernel<kGram, 1, 0>)
+                           : reinterpret_cast<const void*>(&ns_gemm_kernel<kGram, 0, 0>))
+      : mode == kPoly ? (variant ? reinterpret_cast<const void*>(&ns_gemm_kernel<kPoly, 1, 0>)
+                             : reinterpret_cast<const void*>(&ns_gemm_kernel<kPoly, 0, 0>))
+                      : (variant ? reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate, 0, 1>)
+                             : reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate, 0, 0>));
+  const int slot = mode * 2 + variant;
   const int smem = mode == kGram ? GemmShape<kGram>::smem : mode == kPoly ? GemmShape<kPoly>::smem
                                                                          : GemmShape<kUpdate>::smem;
   static int max_pairs[6] = {0, 0, 0, 0, 0, 0};

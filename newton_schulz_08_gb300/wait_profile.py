@@ -15,7 +15,11 @@ ones).  Printed per phase, averaged over CTAs and over the phase's launches:
   tiles          tiles per CTA
   mma_loop       MMA issuer's whole loop (leader CTAs)
 
-Usage: python -m newton_schulz_08_gb300.wait_profile [gpt2|gpt1p5b|rect] [--steps N]
+The Muon step's last update also applies p -= lr O, so its update average
+mixes four plain launches with that one; --ns5 profiles ns5_bank on the same
+bank instead, whose updates are all plain.
+
+Usage: python -m newton_schulz_08_gb300.wait_profile [gpt2|gpt1p5b|rect] [--steps N] [--ns5]
 """
 
 import argparse
@@ -36,20 +40,25 @@ def bank(name):
     return {"gpt2": inputs.gpt2_shapes, "gpt1p5b": inputs.gpt1p5b_shapes, "rect": inputs.rect_shapes}[name]()
 
 
-def profile(shapes, steps=5, ns_steps=5, device="cuda"):
+def profile(shapes, steps=5, ns_steps=5, device="cuda", ns5=False):
     dev = torch.device(device)
     P = [torch.from_numpy(inputs.param(s, i)).to(dev) for i, s in enumerate(shapes)]
     B = [torch.from_numpy(inputs.buffer(s, i)).to(dev) for i, s in enumerate(shapes)]
     G = [torch.from_numpy(inputs.grad(s, i)).to(dev).to(torch.bfloat16) for i, s in enumerate(shapes)]
-    ws = None
+    if ns5:
+        ws = muon.new_workspace(muon.ns5_bank_workspace_size(shapes), dev)
+        run = lambda: muon.ns5_bank(G, ns_steps, workspace=ws)
+    else:
+        ws = muon.muon_step(P, G, B, ns_steps=ns_steps)
+        run = lambda: muon.muon_step(P, G, B, ns_steps=ns_steps, workspace=ws)
     for _ in range(3):
-        ws = muon.muon_step(P, G, B, ns_steps=ns_steps, workspace=ws)
+        run()
     torch.cuda.synchronize(dev)
     counts = torch.zeros(len(PHASES) * MAX_CTAS * len(COUNTERS), dtype=torch.int64, device=dev)
     muon.muon_set_debug("wait_profile_buffer", counts.data_ptr())
     try:
         for _ in range(steps):
-            muon.muon_step(P, G, B, ns_steps=ns_steps, workspace=ws)
+            run()
         torch.cuda.synchronize(dev)
     finally:
         muon.muon_set_debug("wait_profile_buffer", 0)
@@ -73,8 +82,9 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("bank", nargs="?", default="gpt2", choices=["gpt2", "gpt1p5b", "rect"])
     ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--ns5", action="store_true", help="profile ns5_bank (no parameter update)")
     args = ap.parse_args()
-    for phase, d in profile(bank(args.bank), args.steps).items():
+    for phase, d in profile(bank(args.bank), args.steps, ns5=args.ns5).items():
         print(phase, json.dumps({k: round(v, 1) for k, v in d.items()}))
 
 

@@ -50,5 +50,8 @@ def test_elementwise_bytes():
     assert b["momentum_cast"] == 12 * e == pytest.approx(1.019e9, rel=1e-3)
     assert b["normalise"] == 4 * e
     assert b["apply"] == 10 * e
+    # the last update with the parameter update: X and B read, p read and
+    # written (GPT-2 bank: every matrix has m = 768)
+    assert b["update_apply"] == 10 * e + len(shapes) * 2 * 768 ** 2
     b = bench.hbm_bytes(shapes, 2, ns5_only=True)
     assert b["momentum_cast"] == 4 * e and b["apply"] == 4 * e
