@@ -257,7 +257,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // 3-D bf16 map over `count` matrices of rows x cols (row pitch `pitch`).
 bool encode_map(CUtensorMap* map, void* base, int cols, int rows, int count, int pitch, int box_cols,
-                int box_rows) {
+                int box_rows, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
@@ -267,8 +267,8 @@ bool encode_map(CUtensorMap* map, void* base, int cols, int rows, int count, int
   cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // 4-D bf16 map viewing the columns of `count` matrices of rows x cols (row
@@ -431,9 +431,10 @@ muon_status_t run(const std::vector<JobMat>& mats, const Plan& P, float lr, floa
           if (!ok) return MUON_ERR_CUDA;
           // poly: one-copy transposed reads of A where the width allows
           g.t4 = mode == kPoly && sym && encode_map4(&g.tmT4, A, cp.m, cp.m, cp.count, cp.lda);
-          g.out = static_cast<__nv_bfloat16*>(mode == kGram ? A : B);
-          g.ld_out = cp.lda;
-          g.out_mat_stride = static_cast<long long>(cp.m) * cp.lda;
+          // mirrored entries of the Gram (wide A) and the polynomial (B)
+          if (mode != kUpdate && !encode_map(&g.tmMir, mode == kGram ? A : B, cp.m, cp.m, cp.count, cp.lda, 32, 64,
+                                             CU_TENSOR_MAP_SWIZZLE_NONE))
+            return MUON_ERR_CUDA;
           g.m = cp.m;
           g.n = cp.n;
           g.count = cp.count;

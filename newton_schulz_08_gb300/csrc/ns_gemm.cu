@@ -183,6 +183,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         ptx::prefetch_tmap(&P.cls[c].tmOut);
         ptx::prefetch_tmap(&P.cls[c].tmT);
         ptx::prefetch_tmap(&P.cls[c].tmT4);
+        if (MODE != kUpdate) ptx::prefetch_tmap(&P.cls[c].tmMir);
       }
       int stage = 0;
       uint32_t phase = 0;
@@ -522,21 +523,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         }
       }
       if ((MODE == kPoly || (MODE == kGram && !SYM)) && tl.I != tl.J) {
-        // B (and A of wide matrices) is stored whole: mirrored entries
-        // (r, c) -> (c, r) straight from registers, a warp writing 32
-        // adjacent r of one row c (64 contiguous bytes) per store
-        const int rg = tl.I * kBM + rowoff + row_local;
-        if (rg < C.m) {
-          uint16_t* mcol = reinterpret_cast<uint16_t*>(C.out + tl.idx * C.out_mat_stride) + rg;
+        // B (and A of wide matrices) is stored whole: the mirrored entries
+        // (r, c) -> (c, r) of the warp's 32 rows go through its first staging
+        // slot transposed, 64 columns at a time: row c of the slot holds the
+        // 32 values of column c (64 bytes, unswizzled, one store instruction
+        // for the warp), and one TMA box of 64 rows c by 32 columns r takes
+        // them out (clipped at the matrix edge)
+        const uint32_t slot = stg_a + (MODE == kGram ? colhalf : 2 * colhalf) * ((kBM / 2) * 128) + my_rows;
+        const int r0 = tl.I * kBM + rowoff + q * kEpiRows;
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
+        for (int h = 0; h < 2; ++h) {
+          if (lane == 0) ptx::bulk_wait_read0();  // the slot's last store has read it
+          __syncwarp();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int c = tl.J * kBN + colhalf * (kBN / 2) + ch * 32 + j;
-              if (c < C.m)
-                mcol[static_cast<long long>(c) * C.ld_out] =
-                    static_cast<uint16_t>((w[ch][j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
-            }
+          for (int c = 0; c < 64; ++c) {
+            const int ch = 2 * h + (c >> 5), j = c & 31;
+            ptx::sts16(slot + c * 64 + lane * 2, static_cast<uint16_t>(w[ch][j >> 1] >> (16 * (j & 1))));
+          }
+          ptx::fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_3d(&C.tmMir, slot, r0, tl.J * kBN + colhalf * (kBN / 2) + 64 * h, tl.idx);
+            ptx::bulk_commit();
           }
         }
       }

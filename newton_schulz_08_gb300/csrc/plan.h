@@ -91,9 +91,8 @@ struct GemmClass {
                                 //   (MN-major, box 64 x 64)
   CUtensorMap tmT4;             // the same as 4-D (64 columns, rows, 64-column
                                 //   chunk, matrix): both atoms in one copy
-  __nv_bfloat16* out;           // poly: B, for the mirrored writes
-  long long out_mat_stride;     // elements between matrices of out
-  int ld_out;
+  CUtensorMap tmMir;            // Gram (wide A) / poly: the output's mirrored
+                                //   entries, box 32 x 64, unswizzled
   int m, n, count, K;
   int tiles_m, tiles_n, tiles_per_mat;
   int tile_begin;
