@@ -125,6 +125,47 @@ def hbm_bytes(shapes, gbytes, ns5_only=False):
             "update_apply": e * (2 + 4 + 4) + b_bytes}
 
 
+def kernel_report(ktimes, steps, flops, issued_flops, gbytes, peaks):
+    """Per kernel kind: mean launch time, launches per step, achieved rate on
+    the algorithmic work of the launches timed under that kind, fraction of
+    the measured peak and share of the summed kernel time.  ktimes:
+    {kind: (total_ms, launches)} over `steps` steps; flops / issued_flops:
+    FLOPs per step of the GEMM kinds (all NS_STEPS iterations); gbytes:
+    algorithmic bytes per step of the HBM-bound kinds.  When the Muon step's
+    last update is timed as its own kind (update_apply, which also applies
+    p -= lr O), the update kind holds NS_STEPS - 1 of the iterations."""
+    kflops, kissued = dict(flops), dict(issued_flops)
+    if ktimes.get("update_apply", (0, 0))[1]:
+        for f in (kflops, kissued):
+            f["update"] *= (NS_STEPS - 1) / NS_STEPS
+    kern = {}
+    for kind, (tot_ms, cnt) in ktimes.items():
+        if cnt == 0:
+            continue
+        avg = tot_ms / cnt
+        per_step = cnt / steps
+        if kind in kflops:
+            work = kflops[kind] / per_step  # per launch
+            ach = work / (avg * 1e-3) / 1e12
+            issued = kissued[kind] / per_step / (avg * 1e-3) / 1e12
+            kern[kind] = {"avg_ms": avg, "launches_per_step": per_step, "share": None,
+                          "achieved": ach, "unit": "TFLOP/s", "bound": "tensor",
+                          "peak": peaks["bf16_tflops"], "frac": ach / peaks["bf16_tflops"],
+                          "work_per_launch": work, "issued_tflops": issued,
+                          "issued_frac": issued / peaks["bf16_tflops"]}
+        else:
+            work = gbytes[kind] / per_step
+            ach = work / (avg * 1e-3) / 1e9
+            kern[kind] = {"avg_ms": avg, "launches_per_step": per_step, "share": None,
+                          "achieved": ach, "unit": "GB/s", "bound": "hbm",
+                          "peak": peaks["hbm_gbs"], "frac": ach / peaks["hbm_gbs"],
+                          "work_per_launch": work}
+    tot = sum(v["avg_ms"] * v["launches_per_step"] for v in kern.values())
+    for v in kern.values():
+        v["share"] = v["avg_ms"] * v["launches_per_step"] / tot
+    return kern
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -567,37 +608,7 @@ def main():
     peaks, peak_src = load_peaks()
     flops = ns_flops(shapes)
     gbytes = hbm_bytes(shapes, gbytes, ns5_only)
-    # per kind: the work of the launches timed under it (the last of the
-    # NS_STEPS updates is timed as update_apply when the step applies p there)
-    kflops, kissued = dict(flops), ns_flops_issued(shapes)
-    if ktimes.get("update_apply", (0, 0))[1]:
-        for f in (kflops, kissued):
-            f["update"] *= (NS_STEPS - 1) / NS_STEPS
-    kern = {}
-    for kind, (tot_ms, cnt) in ktimes.items():
-        if cnt == 0:
-            continue
-        avg = tot_ms / cnt
-        per_step = cnt / args.steps
-        if kind in kflops:
-            work = kflops[kind] / per_step  # per launch
-            ach = work / (avg * 1e-3) / 1e12
-            issued = kissued[kind] / per_step / (avg * 1e-3) / 1e12
-            kern[kind] = {"avg_ms": avg, "launches_per_step": per_step, "share": None,
-                          "achieved": ach, "unit": "TFLOP/s", "bound": "tensor",
-                          "peak": peaks["bf16_tflops"], "frac": ach / peaks["bf16_tflops"],
-                          "work_per_launch": work, "issued_tflops": issued,
-                          "issued_frac": issued / peaks["bf16_tflops"]}
-        else:
-            work = gbytes[kind] / per_step
-            ach = work / (avg * 1e-3) / 1e9
-            kern[kind] = {"avg_ms": avg, "launches_per_step": per_step, "share": None,
-                          "achieved": ach, "unit": "GB/s", "bound": "hbm",
-                          "peak": peaks["hbm_gbs"], "frac": ach / peaks["hbm_gbs"],
-                          "work_per_launch": work}
-    tot = sum(v["avg_ms"] * v["launches_per_step"] for v in kern.values())
-    for v in kern.values():
-        v["share"] = v["avg_ms"] * v["launches_per_step"] / tot
+    kern = kernel_report(ktimes, args.steps, flops, ns_flops_issued(shapes), gbytes, peaks)
     dom = max(kern, key=lambda k: kern[k]["share"])
     d = kern[dom]
     traffic = None

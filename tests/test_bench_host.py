@@ -55,3 +55,36 @@ def test_elementwise_bytes():
     assert b["update_apply"] == 10 * e + len(shapes) * 2 * 768 ** 2
     b = bench.hbm_bytes(shapes, 2, ns5_only=True)
     assert b["momentum_cast"] == 4 * e and b["apply"] == 4 * e
+
+
+def test_kernel_report_work_per_launch():
+    """Each launch of a Newton-Schulz phase does one iteration's work over
+    the bank; with the last update timed as update_apply, the update kind
+    holds the other NS_STEPS - 1 iterations.  Shares sum to one and each
+    fraction is the achieved rate over its peak."""
+    shapes = bench.workload_shapes("gpt2")
+    flops, issued = bench.ns_flops(shapes), bench.ns_flops_issued(shapes)
+    gbytes = bench.hbm_bytes(shapes, 2)
+    peaks = {"bf16_tflops": 2000.0, "hbm_gbs": 7000.0}
+    steps, ns = 3, bench.NS_STEPS
+    fused = {"momentum_cast": (0.5, steps), "normalise": (0.2, steps), "gram": (1.0, ns * steps),
+             "poly": (0.8, ns * steps), "update": (1.6, (ns - 1) * steps), "update_apply": (0.6, steps),
+             "apply": (0.0, 0)}
+    k = bench.kernel_report(fused, steps, flops, issued, gbytes, peaks)
+    assert "apply" not in k
+    per_iter = flops["update"] / ns
+    assert k["update"]["work_per_launch"] == pytest.approx(per_iter)
+    assert k["update"]["launches_per_step"] == ns - 1
+    assert k["gram"]["work_per_launch"] == pytest.approx(flops["gram"] / ns)
+    assert k["update_apply"]["unit"] == "GB/s" and k["update_apply"]["work_per_launch"] == gbytes["update_apply"]
+    assert sum(v["share"] for v in k.values()) == pytest.approx(1.0)
+    for v in k.values():
+        assert v["frac"] == pytest.approx(v["achieved"] / v["peak"])
+    # the Newton-Schulz-only path: all NS_STEPS updates under one kind
+    plain = dict(fused, update=(2.0, ns * steps), update_apply=(0.0, 0), apply=(0.3, steps))
+    k = bench.kernel_report(plain, steps, flops, issued, gbytes, peaks)
+    assert "update_apply" not in k
+    assert k["update"]["work_per_launch"] == pytest.approx(per_iter)
+    assert k["update"]["issued_tflops"] == pytest.approx(issued["update"] / ns / (2.0 / (ns * steps) * 1e-3) / 1e12)
+    # flops is not modified
+    assert flops == bench.ns_flops(shapes)
