@@ -17,6 +17,10 @@ Source of the method:
 Three steps are not printed on that page; the readings taken here are stated in
 ``oracle.muon`` next to the code that takes them.
 
+``oracle.fp8`` restates the FP8 scaled matrix multiplication (E4M3 forward,
+E5M2 gradients, BF16 results) that the same walk-through page describes in
+section "自定义FP8矩阵乘法实现"; its readings are stated there.
+
 ``oracle.adam`` restates the Adam step with cautious weight decay that the page
 on the modded-nanogpt record "2026-06-11_RecursiveFromBest" (lqnn.cn,
 news/184262, section "3.3 bigram 与 value-embedding 银行上的 C-Optim / 谨慎
@@ -25,10 +29,14 @@ Adam") describes for the embedding-type banks; its readings are stated there.
 Pin status: every public function is pinned by the CPU tests
 (closed form via SVD, invariants, brute force in exact rational arithmetic,
 bit-exact bf16 rounding against an independent routine; for Adam: closed
-forms, torch.optim.Adam / AdamW special cases, hand-worked mask values).
+forms, torch.optim.Adam / AdamW special cases, hand-worked mask values; for
+FP8: bit-exact casts against torch's float8 conversions and a bit-field
+decoding of all 256 codes, exact products of representable operands, power-of-
+two scale invariance, brute force in rational arithmetic).
 """
 
 from .adam import ADAM_DEFAULTS, adam_constants, adam_step, cautious_mask
+from .fp8 import FP8_FORMATS, fp8_mm, fp8_mm_backward, quantize, round_to_fp8
 from .bf16 import round_to_bf16, BF16_MAX
 from .muon import (
     NS_COEFFS,
@@ -47,6 +55,11 @@ from .muon import (
 )
 
 __all__ = [
+    "FP8_FORMATS",
+    "fp8_mm",
+    "fp8_mm_backward",
+    "quantize",
+    "round_to_fp8",
     "ADAM_DEFAULTS",
     "adam_constants",
     "adam_step",

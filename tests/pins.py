@@ -14,6 +14,11 @@ shows up as a disagreement.
   compared in exact rational arithmetic.
 * ``ns_bf16_exact``: the bf16-mode iteration in exact rational arithmetic
   (Python ``fractions``) for tiny matrices, rounding with ``bf16_nearest``.
+* ``fp8_decode`` / ``fp8_nearest``: the 256 codes of the FP8 formats decoded
+  from their bit fields (sign, exponent, fraction), and rounding by search
+  over the finite codes in rational arithmetic (nearest value, ties to the
+  code with an even fraction, overflow past the midpoint above the largest
+  finite value to NaN in E4M3 and to infinity in E5M2).
 """
 
 from decimal import Decimal, getcontext
@@ -133,3 +138,66 @@ def ns_bf16_exact(G, steps, coeffs32, eps=1e-7):
     if tall:
         X = _transpose(X)
     return np.array([[float(v) for v in row] for row in X], dtype=np.float64)
+
+
+# ---------------------------------------------------------------- FP8 codes
+FP8_FIELDS = {"e4m3": (4, 3, 7), "e5m2": (5, 2, 15)}  # exponent bits, fraction bits, bias
+
+
+def fp8_decode(code, fmt):
+    """Value of the 8-bit code in format ``fmt``, from its bit fields: NaN
+    for E4M3's all-ones exponent-and-fraction and E5M2's all-ones exponent
+    with a non-zero fraction, infinity for E5M2's all-ones exponent with a
+    zero fraction."""
+    ebits, fbits, bias = FP8_FIELDS[fmt]
+    sign = -1.0 if code & 0x80 else 1.0
+    e = (code >> fbits) & ((1 << ebits) - 1)
+    f = code & ((1 << fbits) - 1)
+    if fmt == "e4m3" and e == 15 and f == 7:
+        return float("nan")
+    if fmt == "e5m2" and e == 31:
+        return sign * float("inf") if f == 0 else float("nan")
+    if e == 0:
+        return sign * f * 2.0 ** (1 - bias - fbits)
+    return sign * (1 + f / 2.0 ** fbits) * 2.0 ** (e - bias)
+
+
+def _fp8_table(fmt):
+    vals = [(fp8_decode(c, fmt), c) for c in range(0x80)]
+    return sorted((Fraction(v), c) for v, c in vals if np.isfinite(v))
+
+
+_FP8_TABLES = {f: _fp8_table(f) for f in FP8_FIELDS}
+_FP8_NEXT = {"e4m3": Fraction(480), "e5m2": Fraction(65536)}  # where the code above the largest would sit
+
+
+def fp8_nearest(v, fmt):
+    """Nearest value of ``fmt`` to the rational (or float) ``v``."""
+    if isinstance(v, float) and not np.isfinite(v):
+        if np.isnan(v) or fmt == "e4m3":
+            return float("nan")
+        return v
+    v = Fraction(v)
+    sign = -1 if v < 0 else 1
+    a = -v if v < 0 else v
+    table = _FP8_TABLES[fmt]
+    top, top_code = table[-1]
+    if a > top:
+        # a tie goes to the even code: E4M3's largest finite code 0x7E is
+        # even (the tie stays), E5M2's 0x7B is odd (the tie goes to the
+        # infinity code 0x7C)
+        mid = (top + _FP8_NEXT[fmt]) / 2
+        goes_up = a > mid or (a == mid and top_code % 2 == 1)
+        if not goes_up:
+            return sign * float(top)
+        return float("nan") if fmt == "e4m3" else sign * float("inf")
+    lo = max((t for t in table if t[0] <= a), key=lambda t: t[0])
+    hi = min((t for t in table if t[0] >= a), key=lambda t: t[0])
+    if lo[0] == a:
+        return sign * float(lo[0])
+    dlo, dhi = a - lo[0], hi[0] - a
+    if dlo != dhi:
+        r = lo if dlo < dhi else hi
+    else:
+        r = lo if lo[1] % 2 == 0 else hi
+    return sign * float(r[0])
