@@ -237,6 +237,28 @@ typedef struct adam_tensor_desc {
 muon_status_t adam_step(const adam_tensor_desc* tensors, int n_tensors, float lr, float beta1, float beta2,
                         float eps, float weight_decay, int step, int cautious, void* stream);
 
+/* FP8 scaled matrix product, the forward of the page's FP8 matmul
+ * (walk-through page, section "自定义FP8矩阵乘法实现"):
+ *   x_f8 = E4M3(bf16(x / x_s)),  w_f8 = E4M3(bf16(w / w_s)),
+ *   out  = bf16(x_s * w_s * (x_f8 . w_f8^T)), accumulated in fp32.
+ * x: M x K bfloat16, w: N x K bfloat16, row-major, read only.  out: M x N
+ * bfloat16; x_f8: M x K and w_f8: N x K E4M3 bytes (1 sign, 4 exponent, 3
+ * fraction bits, no infinities; 0x7F / 0xFF are NaN), all row-major and
+ * written.  The quotient is rounded once to bfloat16, then to E4M3 to
+ * nearest even; a quotient past E4M3's rounding range (|q| > 464) becomes
+ * NaN.  x_s and w_s: finite and positive.
+ * Limits: K a positive multiple of 16 and N a multiple of 8 (16-byte rows
+ * for the copy engine); M, N, K at most INT_MAX.  M = 0 or N = 0 is a no-op.
+ * All pointers 16-byte aligned; outputs overlap neither each other nor the
+ * inputs.  workspace: at least 256 bytes, 256-byte aligned, holding the
+ * device status word (muon_device_status).  Asynchronous on `stream`;
+ * nothing is allocated.
+ * Returns MUON_OK, MUON_ERR_INVALID_ARG, MUON_ERR_MISALIGNED,
+ * MUON_ERR_ALIASING, MUON_ERR_WORKSPACE_TOO_SMALL, MUON_ERR_TOO_LARGE,
+ * MUON_ERR_UNSUPPORTED_DEVICE or MUON_ERR_CUDA. */
+muon_status_t fp8_mm(const void* x, const void* w, float x_s, float w_s, void* out, void* x_f8, void* w_f8,
+                     int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Assigns each matrix of a bank to one of `world` ranks, for running the
  * step on several GPUs, one process per GPU, each updating only the matrices
  * it owns (every matrix's step depends on that matrix alone, so no data is

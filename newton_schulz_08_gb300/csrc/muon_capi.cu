@@ -20,6 +20,7 @@
 #include <algorithm>
 #include <atomic>
 #include <climits>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -33,6 +34,7 @@ cudaError_t launch_ns_gemm(int mode, int sym, const GemmParams& P, int num_sms, 
 cudaError_t launch_momentum_cast(const K1Params& P, int blocks, cudaStream_t stream);
 cudaError_t launch_normalise(const NormParams& P, int blocks, cudaStream_t stream);
 cudaError_t launch_apply(const ApplyParams& P, int blocks, cudaStream_t stream);
+cudaError_t launch_fp8_quantize(const Fp8QuantParams& P, int blocks, cudaStream_t stream);
 
 namespace {
 
@@ -268,6 +270,21 @@ bool encode_map(CUtensorMap* map, void* base, int cols, int rows, int count, int
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D one-byte map over one rows x cols matrix (row pitch `pitch` bytes),
+// 128-byte swizzle: the FP8 operands.
+bool encode_map_u8(CUtensorMap* map, void* base, long long cols, long long rows, long long pitch, int box_cols,
+                   int box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), 1};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch), static_cast<cuuint64_t>(pitch) * static_cast<cuuint64_t>(rows)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -769,6 +786,77 @@ int muon_kernel_times(double* ms, int* launches, int n_kinds) {
   std::lock_guard<std::mutex> lk(g_ev_mu);
   g_ev_pool.insert(g_ev_pool.end(), pending.begin(), pending.end());
   return rc;
+}
+
+// FP8 scaled product (page section "自定义FP8矩阵乘法实现"): x_f8 =
+// E4M3(bf16(x / x_s)), w_f8 = E4M3(bf16(w / w_s)), out = bf16(x_s w_s
+// (x_f8 . w_f8^T)) with an fp32 accumulator.
+muon_status_t fp8_mm(const void* x, const void* w, float x_s, float w_s, void* out, void* x_f8, void* w_f8,
+                     int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes, void* stream) {
+  if (M < 0 || N < 0 || K < 0) return MUON_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return MUON_OK;
+  if (K == 0 || K % 16 != 0 || N % 8 != 0) return MUON_ERR_INVALID_ARG;
+  if (!x || !w || !out || !x_f8 || !w_f8 || !workspace) return MUON_ERR_INVALID_ARG;
+  if (!(std::isfinite(x_s) && x_s > 0.0f && std::isfinite(w_s) && w_s > 0.0f)) return MUON_ERR_INVALID_ARG;
+  if (M > INT_MAX || N > INT_MAX || K > INT_MAX) return MUON_ERR_TOO_LARGE;
+  if (M * K > (1LL << 40) || N * K > (1LL << 40) || M * N > (1LL << 40)) return MUON_ERR_TOO_LARGE;
+  const long long tm = ceil_div(M, kBM), tn = ceil_div(N, kBN);
+  if (tm * tn > (1LL << 24)) return MUON_ERR_TOO_LARGE;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(out) || !aligned16(x_f8) || !aligned16(w_f8))
+    return MUON_ERR_MISALIGNED;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return MUON_ERR_MISALIGNED;
+  if (workspace_bytes < 256) return MUON_ERR_WORKSPACE_TOO_SMALL;
+  auto at = [](const void* p) { return reinterpret_cast<uintptr_t>(p); };
+  std::vector<Range> ranges = {{at(x), at(x) + 2 * static_cast<uintptr_t>(M * K), false},
+                               {at(w), at(w) + 2 * static_cast<uintptr_t>(N * K), false},
+                               {at(out), at(out) + 2 * static_cast<uintptr_t>(M * N), true},
+                               {at(x_f8), at(x_f8) + static_cast<uintptr_t>(M * K), true},
+                               {at(w_f8), at(w_f8) + static_cast<uintptr_t>(N * K), true},
+                               {at(workspace), at(workspace) + 256, true}};
+  if (ranges_overlap(ranges)) return MUON_ERR_ALIASING;
+  int sms = 0;
+  muon_status_t s = current_device(sms);
+  if (s != MUON_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, 256, st) != cudaSuccess) return MUON_ERR_CUDA;
+
+  Fp8QuantParams q;
+  std::memset(&q, 0, sizeof(q));
+  q.src[0] = static_cast<const __nv_bfloat16*>(x);
+  q.src[1] = static_cast<const __nv_bfloat16*>(w);
+  q.dst[0] = static_cast<uint8_t*>(x_f8);
+  q.dst[1] = static_cast<uint8_t*>(w_f8);
+  q.n[0] = M * K;
+  q.n[1] = N * K;
+  q.scale[0] = x_s;
+  q.scale[1] = w_s;
+  q.blocks0 = ceil_div(M * K, kQuantPerBlock);
+  const long long qblocks = q.blocks0 + ceil_div(N * K, kQuantPerBlock);
+  if (launch_fp8_quantize(q, static_cast<int>(qblocks), st) != cudaSuccess) return MUON_ERR_CUDA;
+
+  GemmParams gp;
+  std::memset(&gp, 0, sizeof(gp));
+  GemmClass& g = gp.cls[0];
+  if (!encode_map_u8(&g.tmA, x_f8, K, M, K, 2 * kBK, kBM / 2) || !encode_map_u8(&g.tmB, w_f8, K, N, K, 2 * kBK, kBN / 2) ||
+      !encode_map(&g.tmOut, out, static_cast<int>(N), static_cast<int>(M), 1, static_cast<int>(N), 64, kEpiRows))
+    return MUON_ERR_CUDA;
+  // the other maps are not read by the FP8 product (only prefetched)
+  g.tmAux = g.tmT = g.tmT4 = g.tmMir = g.tmOut;
+  g.m = static_cast<int>(M);
+  g.n = static_cast<int>(N);
+  g.count = 1;
+  g.K = static_cast<int>(K);
+  g.tiles_m = static_cast<int>(tm);
+  g.tiles_n = static_cast<int>(tn);
+  g.tiles_per_mat = static_cast<int>(tm * tn);
+  gp.n_classes = 1;
+  gp.total_tiles = static_cast<int>(tm * tn);
+  gp.cc = static_cast<float>(static_cast<double>(x_s) * static_cast<double>(w_s));
+  gp.status = static_cast<int*>(workspace);
+  gp.wait_budget = g_wait_budget.load();
+  gp.inject_stall = g_inject_stall.load();
+  if (launch_ns_gemm(kFp8, 0, gp, sms, st) != cudaSuccess) return MUON_ERR_CUDA;
+  return MUON_OK;
 }
 
 }  // extern "C"

@@ -25,6 +25,11 @@
 //             reads X's tile and fuses a X + (.).  In the last step of the
 //             Muon step it applies p <- p - lr X' (fp32, in p's own layout)
 //             instead of storing X'.
+//   kFp8    : out = s (A B^T), the FP8 scaled product of the same page's
+//             section "自定义FP8矩阵乘法实现": A (M x K) and B (N x K) in E4M3,
+//             both K-major (tcgen05.mma kind::f8f6f4, K blocks of 128
+//             one-byte elements, the same 128-byte rows as 64 bf16), s =
+//             x_s w_s applied to the fp32 accumulator, bf16 out.
 //
 // Kernel structure: clusters of two CTAs on neighbouring SMs; each pair
 // computes 256 x 256 output tiles with tcgen05.mma.cta_group::2 (M = 256 over
@@ -72,7 +77,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& P, int t) {
   r.cls = c;
   r.idx = local / C.tiles_per_mat;
   int q = local - r.idx * C.tiles_per_mat;
-  if (MODE == kUpdate) {
+  if (MODE == kUpdate || MODE == kFp8) {
     r.I = q % C.tiles_m;
     r.J = q / C.tiles_m;
   } else {
@@ -120,6 +125,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int kSt = GemmShape<MODE>::stages;
+  // the Gram and the FP8 product stage no epilogue input; an FP8 K block is
+  // 128 one-byte elements (a 128-byte row, as 64 bf16 are)
+  constexpr bool kNoAux = MODE == kGram || MODE == kFp8;
+  constexpr int kKB = MODE == kFp8 ? 2 * kBK : kBK;  // elements per K block
   uint8_t* stg = smem + kSt * kStageBytes;  // epilogue staging tile
   uint64_t* bars = reinterpret_cast<uint64_t*>(stg + GemmShape<MODE>::staging);
   uint64_t* full = bars;                       // leader: both CTAs' tiles landed
@@ -135,7 +144,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const long long t_start = clock64();
-  long long* prof = P.wait_profile ? P.wait_profile + (MODE * 256 + static_cast<long long>(blockIdx.x)) * kWaitCounters
+  long long* prof = P.wait_profile && MODE != kFp8 ? P.wait_profile + (MODE * 256 + static_cast<long long>(blockIdx.x)) * kWaitCounters
                                    : nullptr;
   const uint32_t rank = ptx::cluster_ctarank();  // 0: leader (issues the MMAs)
   const int pair = static_cast<int>(ptx::cluster_id_x());
@@ -192,7 +201,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       for (int t = pair; ok && t < P.total_tiles; t += npairs) {
         const Tile tl = decode_tile<MODE>(P, t);
         const GemmClass& C = P.cls[tl.cls];
-        const int kblocks = (C.K + kBK - 1) / kBK;
+        const int kblocks = (C.K + kKB - 1) / kKB;
         for (int kb = 0; kb < kblocks; ++kb) {
           const long long w0 = prof ? clock64() : 0;
           if (!ptx::mbar_wait(ptx::smem_addr(&empty[stage]), phase ^ 1, budget, abort)) {
@@ -223,7 +232,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           if (MODE == kPoly && SYM && jb < tl.I) {
             load_t(sa, tl.I * kBM + half);
           } else {
-            ptx::tma_load_3d_pair(sa, &C.tmA, fb, kb * kBK, tl.I * kBM + half, tl.idx);
+            ptx::tma_load_3d_pair(sa, &C.tmA, fb, kb * kKB, tl.I * kBM + half, tl.idx);
           }
           if (MODE == kUpdate) {
 #pragma unroll
@@ -233,7 +242,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           } else if (MODE == kPoly && SYM && jb < tl.J) {
             load_t(sb, tl.J * kBN + half);
           } else {
-            ptx::tma_load_3d_pair(sb, &C.tmB, fb, kb * kBK, tl.J * kBN + half, tl.idx);
+            ptx::tma_load_3d_pair(sb, &C.tmB, fb, kb * kKB, tl.J * kBN + half, tl.idx);
           }
           if (++stage == kSt) {
             stage = 0;
@@ -259,7 +268,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       for (int t = pair; ok && t < P.total_tiles; t += npairs, ++it) {
         const Tile tl = decode_tile<MODE>(P, t);
         const GemmClass& C = P.cls[tl.cls];
-        const int kblocks = (C.K + kBK - 1) / kBK;
+        const int kblocks = (C.K + kKB - 1) / kKB;
         const int acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
         const long long w1 = prof ? clock64() : 0;
@@ -291,7 +300,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
                                         : ptx::sdesc_sw128(sa + k * 32, 16, 1024);
             const uint64_t bdesc = b_mn ? ptx::sdesc_sw128(sb + k * 2048, 64 * kBK * 2, 1024)
                                         : ptx::sdesc_sw128(sb + k * 32, 16, 1024);
-            ptx::mma_bf16_pair(d, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
+            if (MODE == kFp8)
+              ptx::mma_f8_pair(d, adesc, bdesc, ptx::idesc_e4m3(kBM, kBN), (kb | k) != 0 ? 1u : 0u);
+            else
+              ptx::mma_bf16_pair(d, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
           }
           ptx::mma_commit_pair_mc(ptx::smem_addr(&empty[stage]), 0x3);
           if (++stage == kSt) {
@@ -345,7 +357,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       }
     };
     auto store_box = [&](const GemmClass& C, const Tile& tl, int bx) {
-      const int sbx = MODE == kGram ? colhalf : bx;
+      const int sbx = kNoAux ? colhalf : bx;
       ptx::tma_store_3d(&C.tmOut, stg_a + sbx * (kBM / 2) * 128 + my_rows, tl.J * kBN + 64 * bx,
                         tl.I * kBM + rowoff + q * kEpiRows, tl.idx);
       ptx::bulk_commit();
@@ -398,7 +410,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         }
       }
     };
-    if (MODE != kGram && lane == 0 && pair < P.total_tiles) load_aux(pair);
+    if (!kNoAux && lane == 0 && pair < P.total_tiles) load_aux(pair);
     uint32_t aux_phase = 0;
     bool ok = true;
     int it = 0;
@@ -416,7 +428,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         pm = static_cast<float*>(mi.out);
         ptall = mi.tall != 0;
       }
-      if (MODE != kGram) {
+      if (!kNoAux) {
         if (!ptx::mbar_wait(ptx::smem_addr(my_aux), aux_phase, budget, abort)) {
           raise_timeout(P, abort);
           ok = false;
@@ -457,9 +469,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         ptx::tmem_ld32(tb + ch * 32, r);
         ptx::tmem_ld_wait();
         // staging box: the tile's 64-column box, or (Gram) the warp's one box
-        const int sbx = MODE == kGram ? colhalf : (c0 >> 6);
+        const int sbx = kNoAux ? colhalf : (c0 >> 6);
         const uint32_t rowa = stg_a + sbx * ((kBM / 2) * 128) + row_local * 128;
-        if (MODE == kGram && ch == 2) {
+        if (kNoAux && ch == 2) {
           // the warp's box still holds its first half until the store has read it
           if (lane == 0) ptx::bulk_wait_read0();
           __syncwarp();
@@ -471,9 +483,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           const uint32_t addr = rowa + ((((j0 + jj) ^ (row_local & 7))) << 4);
           float v[8];
           uint32_t wq[4];
-          if (MODE == kGram) {
+          if (kNoAux) {
+            // Gram: the product; FP8: the product times x_s w_s
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(r[8 * jj + e]);
+            for (int e = 0; e < 8; ++e)
+              v[e] = MODE == kFp8 ? P.cc * __uint_as_float(r[8 * jj + e]) : __uint_as_float(r[8 * jj + e]);
           } else {
             uint32_t x[4];
             ptx::lds128(addr, x[0], x[1], x[2], x[3]);
@@ -556,7 +570,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       }
       if (lane == 0) {
         ptx::bulk_wait_read0();  // this warp's rows are free again
-        if (MODE != kGram && t + npairs < P.total_tiles) {
+        if (!kNoAux && t + npairs < P.total_tiles) {
           ptx::fence_async_smem();
           load_aux(t + npairs);
         }
@@ -568,7 +582,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       }
     }
     if (lane == 0) ptx::bulk_wait0();
-    if (MODE != kGram && lane == 0 && *abort) {
+    if (!kNoAux && lane == 0 && *abort) {
       // an input tile may still be in flight
       ptx::mbar_wait(ptx::smem_addr(my_aux), aux_phase, budget, never);
     }
@@ -597,6 +611,7 @@ template __global__ void ns_gemm_kernel<kPoly, 0, 0>(const __grid_constant__ Gem
 template __global__ void ns_gemm_kernel<kPoly, 1, 0>(const __grid_constant__ GemmParams P);
 template __global__ void ns_gemm_kernel<kUpdate, 0, 0>(const __grid_constant__ GemmParams P);
 template __global__ void ns_gemm_kernel<kUpdate, 0, 1>(const __grid_constant__ GemmParams P);
+template __global__ void ns_gemm_kernel<kFp8, 0, 0>(const __grid_constant__ GemmParams P);
 
 // ------------------------------------------------------------------ launcher
 // Clusters of two CTAs (one pair per cluster), persistent: as many pairs as
@@ -604,18 +619,21 @@ template __global__ void ns_gemm_kernel<kUpdate, 0, 1>(const __grid_constant__ G
 cudaError_t launch_ns_gemm(int mode, int sym, const GemmParams& P, int num_sms, cudaStream_t stream) {
   // Gram / polynomial: 1 = A stored block-upper; update: 1 = with the
   // parameter update
-  const int variant = mode == kUpdate ? (P.apply ? 1 : 0) : (sym ? 1 : 0);
+  const int variant = mode == kUpdate ? (P.apply ? 1 : 0) : mode == kFp8 ? 0 : (sym ? 1 : 0);
   const void* fn =
       mode == kGram ? (variant ? reinterpret_cast<const void*>(&ns_gemm_kernel<kGram, 1, 0>)
                            : reinterpret_cast<const void*>(&ns_gemm_kernel<kGram, 0, 0>))
       : mode == kPoly ? (variant ? reinterpret_cast<const void*>(&ns_gemm_kernel<kPoly, 1, 0>)
                              : reinterpret_cast<const void*>(&ns_gemm_kernel<kPoly, 0, 0>))
-                      : (variant ? reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate, 0, 1>)
-                             : reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate, 0, 0>));
+      : mode == kUpdate ? (variant ? reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate, 0, 1>)
+                                   : reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate, 0, 0>))
+                        : reinterpret_cast<const void*>(&ns_gemm_kernel<kFp8, 0, 0>);
   const int slot = mode * 2 + variant;
-  const int smem = mode == kGram ? GemmShape<kGram>::smem : mode == kPoly ? GemmShape<kPoly>::smem
-                                                                         : GemmShape<kUpdate>::smem;
-  static int max_pairs[6] = {0, 0, 0, 0, 0, 0};
+  const int smem = mode == kGram   ? GemmShape<kGram>::smem
+                   : mode == kPoly ? GemmShape<kPoly>::smem
+                   : mode == kUpdate ? GemmShape<kUpdate>::smem
+                                     : GemmShape<kFp8>::smem;
+  static int max_pairs[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   cudaError_t e = cudaSuccess;
   if (max_pairs[slot] <= 0) {
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

@@ -22,7 +22,7 @@ constexpr int kTallCols = 256;  // momentum pass: a tall matrix's block is 64 ro
 constexpr int kStatusNonFinite = 1;
 constexpr int kStatusTimeout = 2;
 
-enum GemmMode { kGram = 0, kPoly = 1, kUpdate = 2 };
+enum GemmMode { kGram = 0, kPoly = 1, kUpdate = 2, kFp8 = 3 };  // kFp8: out = s * (A B^T), E4M3 operands
 enum FinalMode { kFinalNone = 0, kFinalParam = 1, kFinalOut = 2 };
 
 // One row per matrix of the bank; written by the momentum pass into the
@@ -79,6 +79,18 @@ struct NormParams {
   const MatInfo* table;
   int* status;
 };
+
+// ---------------------------------------------------------------- FP8
+// Operands of the FP8 scaled product: q = E4M3(bf16(src / scale)) for two
+// contiguous bf16 tensors (x and w), 8 elements per thread.
+struct Fp8QuantParams {
+  const __nv_bfloat16* src[2];
+  uint8_t* dst[2];
+  long long n[2];
+  float scale[2];
+  long long blocks0;  // blocks of tensor 0; the rest quantise tensor 1
+};
+constexpr int kQuantPerBlock = 256 * 8;
 
 // ---------------------------------------------------------------- GEMMs
 struct GemmClass {
@@ -173,8 +185,8 @@ constexpr int kSymUpperMaxM = 768;
 
 template <int MODE>
 struct GemmShape {
-  static constexpr int stages = MODE == kGram ? kStages + 1 : kStages;
-  static constexpr int staging = MODE == kGram ? kStageOut / 2 : kStageOut;
+  static constexpr int stages = MODE == kGram || MODE == kFp8 ? kStages + 1 : kStages;
+  static constexpr int staging = MODE == kGram || MODE == kFp8 ? kStageOut / 2 : kStageOut;
   static constexpr int smem = stages * kStageBytes + staging + 1024 /*align*/ + 256 /*barriers*/;
 };
 constexpr int kEpiWarps = 8;     // two warps per TMEM lane quarter, one per column half

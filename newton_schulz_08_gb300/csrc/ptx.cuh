@@ -210,6 +210,17 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, u
       : "memory");
 }
 
+// The same for 8-bit operands (kind::f8f6f4): K = 32 per instruction.
+__device__ __forceinline__ void mma_f8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` in every CTA of `mask` when the pair's MMAs issued so
 // far by this thread are done.
 __device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t mask) {
@@ -278,6 +289,14 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   d |= 1ull << 46;  // descriptor version (tcgen05)
   d |= 2ull << 61;  // swizzle mode: 128 B
   return d;
+}
+
+// Instruction descriptor for kind::f8f6f4 with E4M3 A/B (format code 0),
+// both K-major, and an fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4)                               // D format: f32
+         | (static_cast<uint32_t>(N >> 3) << 17)  // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
 }
 
 // Instruction descriptor for kind::f16 with bf16 A/B and an fp32 accumulator.

@@ -33,7 +33,7 @@ MUON_F32 = 1
 EXPORTS = ["muon_workspace_size", "muon_step", "ns5_workspace_size", "ns5", "ns5_bank",
            "ns5_bank_workspace_size", "muon_device_status", "muon_status_str",
            "ns5_workspace_layout", "muon_set_debug", "muon_kernel_times", "ns5_noalloc",
-           "muon_partition", "adam_step"]
+           "muon_partition", "adam_step", "fp8_mm"]
 
 #: bytes of the static device scratch ns5_noalloc uses (MUON_NOALLOC_SCRATCH_BYTES)
 NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -109,6 +109,8 @@ def lib():
     L.muon_partition.restype = c_int
     L.adam_step.argtypes = [P(adam_tensor_desc), c_int, c_f, c_f, c_f, c_f, c_f, c_int, c_int, c_vp]
     L.adam_step.restype = c_int
+    L.fp8_mm.argtypes = [c_vp, c_vp, c_f, c_f, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_sz, c_vp]
+    L.fp8_mm.restype = c_int
     _lib = L
     return L
 
@@ -313,3 +315,29 @@ def adam_step(params, grads, exp_avgs, exp_avg_sqs, step, lr=1e-3, beta1=0.9, be
     st = lib().adam_step(arr, n, float(lr), float(beta1), float(beta2), float(eps), float(weight_decay),
                          int(step), int(bool(cautious)), _stream(stream))
     _check(st, "adam_step")
+
+
+def fp8_mm(x, w, x_s, w_s, out=None, x_f8=None, w_f8=None, workspace=None, stream=None):
+    """FP8 scaled product of bf16 CUDA tensors x (M x K) and w (N x K):
+    returns (out, x_f8, w_f8), out = bf16(x_s w_s (x_f8 . w_f8^T)) with
+    x_f8 = E4M3(bf16(x / x_s)), w_f8 = E4M3(bf16(w / w_s)) as float8_e4m3fn
+    tensors.  See fp8_mm in include/muon.h."""
+    for t in (x, w):
+        if t.dim() != 2 or t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("x and w must be contiguous 2-D bfloat16 CUDA tensors")
+    M, K = x.shape
+    N = w.shape[0]
+    if w.shape[1] != K:
+        raise ValueError("x and w must have the same number of columns")
+    dev = x.device
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev) if out is None else out
+    x_f8 = torch.empty((M, K), dtype=torch.uint8, device=dev) if x_f8 is None else x_f8.view(torch.uint8)
+    w_f8 = torch.empty((N, K), dtype=torch.uint8, device=dev) if w_f8 is None else w_f8.view(torch.uint8)
+    if workspace is None:
+        workspace = new_workspace(256, dev)
+    st = lib().fp8_mm(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(w.data_ptr()), float(x_s), float(w_s),
+                      ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(x_f8.data_ptr()),
+                      ctypes.c_void_p(w_f8.data_ptr()), M, N, K, ctypes.c_void_p(workspace.data_ptr()),
+                      workspace.numel(), _stream(stream))
+    _check(st, "fp8_mm")
+    return out, x_f8.view(torch.float8_e4m3fn), w_f8.view(torch.float8_e4m3fn)

@@ -185,3 +185,31 @@ def test_set_debug_keys(L):
     assert L.muon_set_debug(b"wait_budget_cycles", 4000000000) == 0
     assert L.muon_set_debug(b"inject_stall", 0) == 0
     assert L.muon_set_debug(b"record_kernel_events", 0) == 0
+
+
+# ------------------------------------------------------------------ fp8_mm
+FX, FW, FO, FXQ, FWQ, FWS = (0x7F0000000000 + k * 0x10000000 for k in range(6))
+
+
+def fp8_call(L, M=256, N=256, K=256, x_s=0.01, w_s=0.02, x=FX, w=FW, out=FO, xq=FXQ, wq=FWQ, ws=FWS, wsb=256):
+    c = ctypes.c_void_p
+    return L.fp8_mm(c(x), c(w), x_s, w_s, c(out), c(xq), c(wq), M, N, K, c(ws), wsb, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(K=24), "INVALID_ARG"), (dict(K=0), "INVALID_ARG"), (dict(N=12), "INVALID_ARG"),
+    (dict(M=-1), "INVALID_ARG"), (dict(x=0), "INVALID_ARG"), (dict(wq=0), "INVALID_ARG"),
+    (dict(ws=0), "INVALID_ARG"), (dict(x_s=0.0), "INVALID_ARG"), (dict(w_s=-1.0), "INVALID_ARG"),
+    (dict(x_s=float("inf")), "INVALID_ARG"), (dict(w_s=float("nan")), "INVALID_ARG"),
+    (dict(x=FX + 8), "MISALIGNED"), (dict(xq=FXQ + 4), "MISALIGNED"), (dict(ws=FWS + 16), "MISALIGNED"),
+    (dict(wsb=128), "WORKSPACE_TOO_SMALL"), (dict(M=1 << 31), "TOO_LARGE"),
+    (dict(out=FX + 256), "ALIASING"), (dict(wq=FXQ + 4096), "ALIASING"), (dict(ws=FO), "ALIASING"),
+])
+def test_fp8_mm_argument_errors(L, kw, code):
+    """Every case is rejected before any CUDA call (fake device addresses)."""
+    assert fp8_call(L, **kw) == getattr(muon, "MUON_ERR_" + code)
+
+
+def test_fp8_mm_empty_is_a_no_op(L):
+    assert fp8_call(L, M=0) == muon.MUON_OK
+    assert fp8_call(L, N=0, x=0) == muon.MUON_OK
