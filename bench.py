@@ -48,6 +48,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # ------------------------------------------------------------------ workloads
 def workload_shapes(name):
     from newton_schulz_08_gb300 import inputs
+    if name == "fp8":
+        return [FP8_SHAPE]
     if name == "adam":
         return inputs.adam_bank_shapes()
     return {
@@ -75,7 +77,10 @@ WORKLOAD_DESC = {
                "G = U diag(s) V^T, s log-uniform in [1e-4, 1]",
     "adam": "Adam step with cautious weight decay on an embedding-type bank: 4 tables of 50304x768, "
             "154.53M fp32 params, bf16 grads, fp32 moments, step 10 of training",
+    "fp8": "FP8 scaled product (forward of the page's FP8 matmul): x 65536x768 bf16 (64 x 1024 tokens of "
+           "GPT-2-124M), w 3072x768 bf16 (its MLP input projection), E4M3 operands, bf16 out",
 }
+FP8_SHAPE = (65536, 3072, 768)  # M (tokens), N (outputs), K (inputs)
 
 
 def ns_flops(shapes, steps=NS_STEPS):
@@ -290,6 +295,29 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     shapes = workload_shapes(args.workload)
+    if args.workload == "fp8":
+        # each step: the oracle's product on a row sample sized to ~1 s
+        budget = max(0.2, 60.0 / max(1, args.steps + args.warmup))
+        for _ in range(args.warmup):
+            fp8_oracle_sample(budget)
+        total_f, total_t = 0.0, 0.0
+        for _ in range(args.steps):
+            f, t = fp8_oracle_sample(budget)
+            total_f += f
+            total_t += t
+        value = total_f / total_t / 1e12
+        line = {
+            "impl": "reference", "metric": "fp8_mm_tflops", "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * total_t / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64 (E4M3-emulating)", "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC[args.workload]},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+                             "sample": "leading rows of x against all of w per step (FP8 oracle)"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(line), flush=True)
+        return
     if args.workload in ADAM_WORKLOADS:
         for _ in range(args.warmup):
             adam_oracle_sample(shapes, 0.0)
@@ -484,6 +512,9 @@ def main():
 
     if args.workload in ADAM_WORKLOADS:
         run_adam(args, rank, world, device)
+        return
+    if args.workload == "fp8":
+        run_fp8(args, rank, world, device)
         return
 
     L = muon.lib()
@@ -762,6 +793,142 @@ def run_adam(args, rank, world, device):
                                 "kind": "oracle",
                                 "sample": f"{n_cpu} params (whole tables in bank order), float32 oracle, "
                                           f"{t_cpu:.1f} s"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def fp8_operands(seed=0):
+    """Seeded bf16 operands of the FP8 workload and per-tensor scales that
+    fill E4M3 (largest |x| / x_s = 448 / 1.05)."""
+    M, N, K = FP8_SHAPE
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    x_s = float(np.abs(x).max() / 448.0 * 1.05)
+    w_s = float(np.abs(w).max() / 448.0 * 1.05)
+    return x, w, x_s, w_s
+
+
+def fp8_oracle_sample(budget_s):
+    """The oracle's FP8 product on the first rows of x, doubling the rows
+    until the budget is spent; returns (FLOPs, seconds)."""
+    import oracle
+    x, w, x_s, w_s = fp8_operands()
+    xb, wb = oracle.round_to_bf16(x), oracle.round_to_bf16(w)
+    N, K = w.shape
+    rows, flops, t = 16, 0.0, 0.0
+    while t < budget_s and rows <= x.shape[0]:
+        t0 = time.perf_counter()
+        oracle.fp8_mm(xb[:rows], wb, x_s, w_s)
+        t += time.perf_counter() - t0
+        flops += 2.0 * rows * N * K
+        rows *= 2
+    return flops, t
+
+
+def run_fp8(args, rank, world, device):
+    """The FP8 scaled product (fp8_mm: quantise pass + tcgen05 kind::f8f6f4
+    product) on one GPT-2-124M MLP projection's worth of tokens; each rank
+    runs its own copy (weak scaling)."""
+    import torch
+    import torch.distributed as dist
+
+    from newton_schulz_08_gb300 import muon
+
+    M, N, K = FP8_SHAPE
+    x, w, x_s, w_s = fp8_operands(rank)
+    X = torch.from_numpy(x).to(device).to(torch.bfloat16)
+    W = torch.from_numpy(w).to(device).to(torch.bfloat16)
+    O = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+    XQ = torch.empty((M, K), dtype=torch.uint8, device=device)
+    WQ = torch.empty((N, K), dtype=torch.uint8, device=device)
+    ws = muon.new_workspace(256, device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(Xi=X, Wi=W):
+        muon.fp8_mm(Xi, Wi, x_s, w_s, out=O, x_f8=XQ, w_f8=WQ, workspace=ws, stream=stream)
+
+    def barrier():
+        torch.cuda.synchronize(device)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(device)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, device)
+    muon.muon_set_debug("record_kernel_events", 1)
+    muon.muon_kernel_times()
+    for _ in range(args.steps):
+        step()
+    barrier()
+    kt = muon.muon_kernel_times()
+    muon.muon_set_debug("record_kernel_events", 0)
+    # e2e: x and w in from pinned host memory, out back
+    in_host = [[X.cpu().pin_memory(), W.cpu().pin_memory()]]
+    bufs = [[X, W], [torch.empty_like(X), torch.empty_like(W)]]
+    o_host = [torch.empty(O.shape, dtype=O.dtype).pin_memory()]
+    barrier()
+    e2e_ms = e2e_pipelined(stream, device, max(3, args.steps // 4), bufs, in_host,
+                           lambda j: step(bufs[j][0], bufs[j][1]), [O], o_host)
+    barrier()
+    clk = clocks.stop()
+    e2e_ms = max_over_ranks(e2e_ms, world, device)
+    st = muon.muon_device_status(ws)
+    if st != 0:
+        raise muon.MuonError(st, "device status after timing")
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    flops = 2.0 * M * N * K
+    fp8_peak = 2.0 * peaks["bf16_tflops"]  # nominal dense FP8 : BF16 rate = 4.5 : 2.25
+    g_ms, g_n = kt["fp8_mm"]
+    q_ms, q_n = kt["fp8_quantize"]
+    g_avg, q_avg = g_ms / g_n, q_ms / q_n
+    ach = flops / (g_avg * 1e-3) / 1e12
+    q_bytes = 3.0 * (M + N) * K  # bf16 in, E4M3 out
+    line = {
+        "metric": "fp8_mm_tflops", "value": flops * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC["fp8"], "M": M, "N": N, "K": K, "x_s": x_s, "w_s": w_s,
+                   "l2": "no flush: x (101 MB bf16) and out (403 MB bf16) exceed the 129 MB L2",
+                   "parallelism": f"{world} ranks, one product each" if world > 1 else "1 GPU"},
+        "roofline": {"kernel": "fp8_mm", "bound": "tensor", "achieved": ach, "peak": fp8_peak, "unit": "TFLOP/s",
+                     "frac": ach / fp8_peak, "traffic": None,
+                     "peak_source": f"{peak_src} bf16_tflops burst x 2 (nominal FP8 : BF16 dense rate)"},
+        "kernels": {"fp8_quantize": {"avg_ms": q_avg, "achieved": q_bytes / (q_avg * 1e-3) / 1e9, "unit": "GB/s",
+                                     "bound": "hbm", "peak": peaks["hbm_gbs"],
+                                     "frac": q_bytes / (q_avg * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+                    "fp8_mm": {"avg_ms": g_avg, "achieved": ach, "unit": "TFLOP/s", "bound": "tensor",
+                               "peak": fp8_peak, "frac": ach / fp8_peak}},
+        "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": int(X.numel() * 2 + W.numel() * 2),
+                "d2h_bytes_per_step": int(O.numel() * 2), "method": E2E_NOTE},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        f_cpu, t_cpu = fp8_oracle_sample(args.cpu_budget)
+        line["cpu_baseline"] = {"value": f_cpu / t_cpu / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(),
+                                "kind": "oracle",
+                                "sample": f"{f_cpu / 2 / N / K:.0f} rows of x against all of w, FP8 oracle "
+                                          f"(float64 matmul), {t_cpu:.1f} s"}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

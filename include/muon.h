@@ -163,7 +163,8 @@ int muon_set_debug(const char* key, long long value);
  * 2 Gram (A = X X^T), 3 polynomial (B = b A + c A A), 4 update
  * (X = a X + B X), 5 apply (O written by ns5, or p <- p - lr O for a step
  * with no iteration), 6 muon_step's last update (X = a X + B X with
- * p <- p - lr O applied in place of storing X).  ms and launches are host
+ * p <- p - lr O applied in place of storing X), 7 fp8_mm's quantise pass,
+ * 8 fp8_mm's product.  ms and launches are host
  * arrays of n_kinds entries; kinds at or above n_kinds are not reported.
  * Returns 0, or -1 on a bad argument or a failed event query. */
 int muon_kernel_times(double* ms, int* launches, int n_kinds);

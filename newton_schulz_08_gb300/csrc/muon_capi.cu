@@ -53,7 +53,8 @@ std::atomic<long long> g_wait_profile{0};  // device address of the counters, 0:
 
 // Optional CUDA-event brackets around every launch (diagnostics).
 // kinds: 0 momentum_cast, 1 normalise, 2 gram, 3 poly, 4 update, 5 apply,
-// 6 the Muon step's last update (p <- p - lr O applied in its epilogue)
+// 6 the Muon step's last update (p <- p - lr O applied in its epilogue),
+// 7 fp8_quantize, 8 the FP8 scaled product
 struct EventPair {
   cudaEvent_t start, stop;
   int kind;
@@ -832,7 +833,10 @@ muon_status_t fp8_mm(const void* x, const void* w, float x_s, float w_s, void* o
   q.scale[1] = w_s;
   q.blocks0 = ceil_div(M * K, kQuantPerBlock);
   const long long qblocks = q.blocks0 + ceil_div(N * K, kQuantPerBlock);
+  EventPair evq;
+  const bool recq = ev_begin(evq, 7, st);
   if (launch_fp8_quantize(q, static_cast<int>(qblocks), st) != cudaSuccess) return MUON_ERR_CUDA;
+  ev_end(evq, recq, st);
 
   GemmParams gp;
   std::memset(&gp, 0, sizeof(gp));
@@ -855,7 +859,10 @@ muon_status_t fp8_mm(const void* x, const void* w, float x_s, float w_s, void* o
   gp.status = static_cast<int*>(workspace);
   gp.wait_budget = g_wait_budget.load();
   gp.inject_stall = g_inject_stall.load();
+  EventPair evg;
+  const bool recg = ev_begin(evg, 8, st);
   if (launch_ns_gemm(kFp8, 0, gp, sms, st) != cudaSuccess) return MUON_ERR_CUDA;
+  ev_end(evg, recg, st);
   return MUON_OK;
 }
 

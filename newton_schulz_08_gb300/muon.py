@@ -39,7 +39,8 @@ EXPORTS = ["muon_workspace_size", "muon_step", "ns5_workspace_size", "ns5", "ns5
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 #: kernel kinds reported by muon_kernel_times
-KERNEL_KINDS = ["momentum_cast", "normalise", "gram", "poly", "update", "apply", "update_apply"]
+KERNEL_KINDS = ["momentum_cast", "normalise", "gram", "poly", "update", "apply", "update_apply", "fp8_quantize",
+                "fp8_mm"]
 
 
 class MuonError(RuntimeError):
