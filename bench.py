@@ -818,13 +818,14 @@ def fp8_oracle_sample(budget_s):
     xb, wb = oracle.round_to_bf16(x), oracle.round_to_bf16(w)
     N, K = w.shape
     rows, flops, t = 16, 0.0, 0.0
-    while t < budget_s and rows <= x.shape[0]:
+    while True:  # at least one chunk
         t0 = time.perf_counter()
         oracle.fp8_mm(xb[:rows], wb, x_s, w_s)
         t += time.perf_counter() - t0
         flops += 2.0 * rows * N * K
         rows *= 2
-    return flops, t
+        if t >= budget_s or rows > x.shape[0]:
+            return flops, t
 
 
 def run_fp8(args, rank, world, device):

@@ -117,7 +117,7 @@ struct GemmParams {
   GemmClass cls[kMaxClasses];
   int n_classes;
   int total_tiles;
-  float ca, cb, cc;             // Newton-Schulz coefficients
+  float ca, cb, cc;             // Newton-Schulz coefficients (kFp8: cc = x_s w_s)
   int* status;
   long long wait_budget;        // clock64 cycles per barrier wait
   int inject_stall;             // test hook: MMA warp issues nothing

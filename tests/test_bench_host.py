@@ -3,6 +3,7 @@ Newton-Schulz FLOPs and elementwise bytes per step, against the figures the
 closed forms give for the benchmark banks, and the issued-MMA count against
 a direct tile enumeration."""
 
+import numpy as np
 import pytest
 
 import bench
@@ -88,3 +89,17 @@ def test_kernel_report_work_per_launch():
     assert k["update"]["issued_tflops"] == pytest.approx(issued["update"] / ns / (2.0 / (ns * steps) * 1e-3) / 1e12)
     # flops is not modified
     assert flops == bench.ns_flops(shapes)
+
+
+def test_fp8_workload_operands_and_oracle_sample():
+    """The FP8 workload's operands fill E4M3 without overflow, x and its
+    output exceed the 129 MB L2, and the oracle sample counts 2 N K FLOPs
+    per row."""
+    M, N, K = bench.FP8_SHAPE
+    assert M * K * 2 > 129e6 / 2 and M * N * 2 > 129e6
+    assert K % 16 == 0 and N % 8 == 0
+    x, w, x_s, w_s = bench.fp8_operands(0)
+    assert x.shape == (M, K) and w.shape == (N, K)
+    assert np.abs(x).max() / x_s < 448 and np.abs(w).max() / w_s < 448
+    f, t = bench.fp8_oracle_sample(0.0)
+    assert f == 2.0 * 16 * N * K and t > 0
