@@ -219,14 +219,17 @@ def ns5_bank(Gs, ns_steps=5, outs=None, workspace=None, stream=None):
     n = len(Gs)
     if outs is None:
         outs = [torch.empty(g.shape, dtype=torch.bfloat16, device=g.device) for g in Gs]
+    if len(outs) != n:
+        raise ValueError("outs must have one tensor per G")
+    for g, o in zip(Gs, outs):
+        if (g.dim() != 2 or not g.is_contiguous() or o.shape != g.shape or o.dtype != torch.bfloat16
+                or not o.is_contiguous()):
+            raise ValueError("each G must be 2-D contiguous with a contiguous bf16 out of the same shape")
     gp = (ctypes.c_void_p * max(n, 1))(*[g.data_ptr() for g in Gs])
     op = (ctypes.c_void_p * max(n, 1))(*[o.data_ptr() for o in outs])
     dt = (ctypes.c_int32 * max(n, 1))(*[_dtype_code(g) for g in Gs])
     rows = (ctypes.c_int64 * max(n, 1))(*[g.shape[0] for g in Gs])
     cols = (ctypes.c_int64 * max(n, 1))(*[g.shape[1] for g in Gs])
-    for g, o in zip(Gs, outs):
-        if g.dim() != 2 or not g.is_contiguous() or o.shape != g.shape or o.dtype != torch.bfloat16:
-            raise ValueError("each G must be 2-D contiguous with a bf16 out of the same shape")
     if workspace is None:
         workspace = new_workspace(lib().ns5_bank_workspace_size(rows, cols, n) if n else 256,
                                   Gs[0].device if n else None)
@@ -332,8 +335,19 @@ def fp8_mm(x, w, x_s, w_s, out=None, x_f8=None, w_f8=None, workspace=None, strea
         raise ValueError("x and w must have the same number of columns")
     dev = x.device
     out = torch.empty((M, N), dtype=torch.bfloat16, device=dev) if out is None else out
-    x_f8 = torch.empty((M, K), dtype=torch.uint8, device=dev) if x_f8 is None else x_f8.view(torch.uint8)
-    w_f8 = torch.empty((N, K), dtype=torch.uint8, device=dev) if w_f8 is None else w_f8.view(torch.uint8)
+    x_f8 = torch.empty((M, K), dtype=torch.uint8, device=dev) if x_f8 is None else x_f8
+    w_f8 = torch.empty((N, K), dtype=torch.uint8, device=dev) if w_f8 is None else w_f8
+    # the library writes exactly these sizes: check the caller's buffers
+    if out.shape != (M, N) or out.dtype != torch.bfloat16 or not out.is_contiguous() or out.device != dev:
+        raise ValueError("out must be a contiguous M x N bfloat16 tensor on x's device")
+    for t, shape in ((x_f8, (M, K)), (w_f8, (N, K))):
+        if (t.shape != shape or t.element_size() != 1 or not t.is_contiguous() or t.device != dev
+                or t.dtype not in (torch.uint8, torch.float8_e4m3fn)):
+            raise ValueError("x_f8 / w_f8 must be contiguous one-byte (uint8 or float8_e4m3fn) tensors "
+                             "shaped like x / w, on x's device")
+    x_f8, w_f8 = x_f8.view(torch.uint8), w_f8.view(torch.uint8)
+    if w.device != dev:
+        raise ValueError("x and w must be on the same device")
     if workspace is None:
         workspace = new_workspace(256, dev)
     st = lib().fp8_mm(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(w.data_ptr()), float(x_s), float(w_s),

@@ -213,3 +213,24 @@ def test_fp8_mm_argument_errors(L, kw, code):
 def test_fp8_mm_empty_is_a_no_op(L):
     assert fp8_call(L, M=0) == muon.MUON_OK
     assert fp8_call(L, N=0, x=0) == muon.MUON_OK
+
+
+def test_fp8_mm_binding_rejects_bad_tensors():
+    """Argument checks of the binding, before any library call."""
+    import torch
+    x = torch.zeros((4, 16), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        muon.fp8_mm(x, x, 1.0, 1.0)  # not CUDA tensors
+    with pytest.raises(ValueError):
+        muon.fp8_mm(x.float(), x, 1.0, 1.0)  # not bfloat16
+
+
+def test_ns5_bank_binding_checks_outs():
+    import torch
+    G = [torch.zeros((4, 8)), torch.zeros((8, 4))]
+    with pytest.raises(ValueError):
+        muon.ns5_bank(G, 5, outs=[torch.zeros((4, 8), dtype=torch.bfloat16)])  # one out for two G
+    with pytest.raises(ValueError):
+        muon.ns5_bank(G, 5, outs=[torch.zeros((4, 8), dtype=torch.bfloat16), torch.zeros((4, 8), dtype=torch.bfloat16)])
+    with pytest.raises(ValueError):
+        muon.ns5_bank([torch.zeros(8)], 5)  # not 2-D
