@@ -207,6 +207,29 @@ def test_backward_of_representable_operands():
     assert gx.shape == (M, K) and gw.shape == (N, K)
 
 
+def test_backward_matches_brute_force_in_rationals():
+    """E5M2 gradient quantised by exhaustive search (after the bf16 quotient,
+    itself by table search), products summed in rationals, each result
+    rounded to bf16 by table search: nothing shared with the oracle."""
+    rng = np.random.default_rng(89)
+    M, N, K = 3, 4, 5
+    gs, xs, ws = 3.7e-6, 0.013, 0.021
+    g = oracle.round_to_bf16(rng.standard_normal((M, N)) * 1e-3)
+    x_f8 = representable(rng, (M, K), "e4m3")
+    w_f8 = representable(rng, (N, K), "e4m3")
+    gx, gw, _ = oracle.fp8_mm_backward(g, x_f8, w_f8, xs, ws, gs)
+    gq = [[Fraction(pins.fp8_nearest(pins.bf16_nearest(Fraction(float(g[i][j])) / Fraction(gs)), "e5m2"))
+           for j in range(N)] for i in range(M)]
+    X = [[Fraction(float(v)) for v in row] for row in x_f8]
+    W = [[Fraction(float(v)) for v in row] for row in w_f8]
+    sx, sw = Fraction(gs) * Fraction(ws), Fraction(gs) * Fraction(xs)
+    want_x = np.array([[pins.bf16_nearest(sx * sum((gq[i][n] * W[n][k] for n in range(N)), Fraction(0)))
+                        for k in range(K)] for i in range(M)])
+    want_w = np.array([[pins.bf16_nearest(sw * sum((gq[m][n] * X[m][k] for m in range(M)), Fraction(0)))
+                        for k in range(K)] for n in range(N)])
+    assert same(gx, want_x) and same(gw, want_w)
+
+
 def test_backward_gradients_approximate_the_unquantised_ones():
     """With scales that fill the formats, the FP8 gradients of out = x w^T
     stay within a few per cent of the exact ones (E5M2 keeps 3 significant
@@ -230,6 +253,7 @@ def _run_pins():
         lambda: test_mm_of_representable_operands_is_the_rounded_exact_product() is None,
         lambda: test_mm_matches_brute_force_in_rationals() is None,
         lambda: test_backward_of_representable_operands() is None,
+        lambda: test_backward_matches_brute_force_in_rationals() is None,
         lambda: test_quantize_follows_the_page_cast_of_a_bfloat16_tensor() is None,
     ]
     failures = 0
