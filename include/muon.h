@@ -31,8 +31,12 @@
  *   - Calls are asynchronous on `stream` and never synchronise, except
  *     muon_device_status().  A workspace must not be shared by calls that
  *     may overlap on the GPU.
- *   - Arguments are checked on the host before anything is launched; on any
- *     error code nothing has been enqueued and no buffer has been touched.
+ *   - Arguments are checked, and every launch is prepared (tensor maps
+ *     encoded, grids sized), on the host before anything is enqueued: on
+ *     any error code nothing has been enqueued and no buffer has been
+ *     touched -- except when the CUDA runtime itself rejects a kernel launch
+ *     (MUON_ERR_CUDA), after which earlier kernels of the same call may have
+ *     been enqueued.
  *   - Device-side conditions (a non-finite norm, an expired bounded wait)
  *     are recorded in the workspace's status word and are read with
  *     muon_device_status().
@@ -111,8 +115,24 @@ size_t ns5_bank_workspace_size(const int64_t* rows, const int64_t* cols, int n_m
 
 /* Synchronises `stream`, then reads the status word of `workspace` left by
  * the last call that used it: MUON_OK, MUON_WARN_NONFINITE or
- * MUON_ERR_DEVICE_TIMEOUT (MUON_ERR_CUDA if the synchronisation failed). */
+ * MUON_ERR_DEVICE_TIMEOUT (MUON_ERR_CUDA if the synchronisation failed).
+ * The word lives in the caller's workspace, so the workspace names the call
+ * whose status is read (calls on one stream may use different workspaces). */
 muon_status_t muon_device_status(const void* workspace, void* stream);
+
+/* Prepared calls.  muon_step, ns5, ns5_bank and ns5_noalloc keep the
+ * prepared launches of recent calls in host memory (at most 32; the least
+ * recently used is dropped), keyed by the current device, the entry point,
+ * ns_steps, the workspace address and every pointer and shape argument.
+ * lr, momentum and nesterov are not part of the key.  A call with a known
+ * key only checks workspace_bytes and enqueues: the planning, the checks
+ * that depend on the key alone, the tensor-map encoding and the occupancy
+ * queries are skipped.  A prepared call depends on nothing but its key, so
+ * it stays valid when the caller frees memory and allocates it again at the
+ * same addresses.  muon_plan_cache_clear() drops every prepared call (for
+ * example to return the host memory); it is never needed for correctness.
+ * Thread-safe. */
+void muon_plan_cache_clear(void);
 
 /* Static description of a status code. */
 const char* muon_status_str(muon_status_t status);
@@ -153,7 +173,10 @@ muon_status_t ns5_workspace_layout(int batch, int64_t rows, int64_t cols, muon_w
  *   "record_kernel_events" 1: every kernel launch is bracketed by a pair of
  *                         CUDA events recorded on the caller's stream (read
  *                         with muon_kernel_times; not for use under stream
- *                         capture).
+ *                         capture);
+ *   "fail_tensor_map_encode" 1: every tensor-map encoding fails, and no
+ *                         prepared call is used or kept (tests that a
+ *                         failure while preparing enqueues nothing).
  * Returns 0 on success, -1 for an unknown key. */
 int muon_set_debug(const char* key, long long value);
 
@@ -164,7 +187,8 @@ int muon_set_debug(const char* key, long long value);
  * (X = a X + B X), 5 apply (O written by ns5, or p <- p - lr O for a step
  * with no iteration), 6 muon_step's last update (X = a X + B X with
  * p <- p - lr O applied in place of storing X), 7 fp8_mm's quantise pass,
- * 8 fp8_mm's product.  ms and launches are host
+ * 8 fp8_mm's product, 9 fp8_mm_backward's quantise-and-transpose pass,
+ * 10 its two products (one launch), 11 its split-K reduction.  ms and launches are host
  * arrays of n_kinds entries; kinds at or above n_kinds are not reported.
  * Returns 0, or -1 on a bad argument or a failed event query. */
 int muon_kernel_times(double* ms, int* launches, int n_kinds);
@@ -182,9 +206,14 @@ int muon_kernel_times(double* ms, int* launches, int n_kinds);
  * The scratch ns5 would take from a workspace comes instead from one
  * file-scope device array of MUON_NOALLOC_SCRATCH_BYTES (64 MiB).  That array
  * occupies device memory on every GPU where the library's device code is
- * loaded until the process exits.  Its device address is looked up on the
- * first call made on each device (make that first call before any stream
- * capture on that device).  Calls whose workspace need
+ * loaded until the process exits.  CUDA loads the library's device code
+ * lazily: the first call made on a device loads it and reserves the array
+ * there, which can fail with MUON_ERR_CUDA when the device is full, so make
+ * one call at initialisation, before any stream capture on that device.
+ * The array's address is looked up on every call with the caller's device
+ * current (it can move after cudaDeviceReset); a device other than compute
+ * capability 10.3 gets MUON_ERR_UNSUPPORTED_DEVICE before anything is
+ * loaded.  Calls whose workspace need
  * (ns5_workspace_size(batch, rows, cols)) exceeds the array return
  * MUON_ERR_SCRATCH_LIMIT without launching anything; for example one 2048 x
  * 2048 matrix or up to seven 1024 x 1024 matrices fit.  Every call shares the
@@ -259,6 +288,44 @@ muon_status_t adam_step(const adam_tensor_desc* tensors, int n_tensors, float lr
  * MUON_ERR_UNSUPPORTED_DEVICE or MUON_ERR_CUDA. */
 muon_status_t fp8_mm(const void* x, const void* w, float x_s, float w_s, void* out, void* x_f8, void* w_f8,
                      int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace fp8_mm_backward needs for these sizes (0 on invalid
+ * sizes, 256 when a size is 0). */
+size_t fp8_mm_backward_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/* Backward of the FP8 scaled product (walk-through page, section
+ * "自定义FP8矩阵乘法实现", subsection "反向传播优化"): the output gradient is
+ * cast to E5M2, which keeps a wider range than E4M3, and multiplied with the
+ * forward's E4M3 operands:
+ *   g_f8   = E5M2(bf16(g / grad_s)),
+ *   grad_x = bf16(grad_s * w_s * (g_f8 . w_f8)),      M x K,
+ *   grad_w = bf16(grad_s * x_s * (g_f8^T . x_f8)),    N x K,
+ * products accumulated in fp32.  As on the page, the products read
+ * transposed copies of g_f8, x_f8 and w_f8 (made in the workspace by one
+ * pass that also quantises g), so both operands of every product are
+ * K-major; the E5M2 x E4M3 products run on the tensor cores.  When the
+ * grad_w product has few output tiles, its contraction over the M rows is
+ * split into slices whose fp32 partial sums are added in slice order.
+ * g: M x N bfloat16; x_f8: M x K and w_f8: N x K E4M3 codes (as fp8_mm
+ * writes them), read only.  grad_x: M x K and grad_w: N x K bfloat16, and
+ * g_f8: M x N E5M2 codes (1 sign, 5 exponent, 2 fraction bits; 0x7C / 0xFC
+ * are infinities, 0x7D-0x7F / 0xFD-0xFF NaN), written.  The quotient is
+ * rounded once to bfloat16, then to E5M2 to nearest even; from 61440 in
+ * magnitude on (the midpoint between 57344 and 2^16) it becomes an infinity
+ * of its sign.  x_s, w_s, grad_s: finite and positive.
+ * Limits: M, N, K multiples of 16 (16-byte rows of every operand and copy),
+ * at most INT_MAX.  K = 0 is a no-op; M = 0 or N = 0 writes zeros to the
+ * other gradient (an empty sum).  All pointers 16-byte aligned; outputs
+ * overlap neither each other, the inputs nor the workspace.  workspace:
+ * fp8_mm_backward_workspace_size(M, N, K) bytes, 256-byte aligned (status
+ * word, the transposed copies, the partial sums).  Asynchronous on
+ * `stream`; nothing is allocated.
+ * Returns MUON_OK, MUON_ERR_INVALID_ARG, MUON_ERR_MISALIGNED,
+ * MUON_ERR_ALIASING, MUON_ERR_WORKSPACE_TOO_SMALL, MUON_ERR_TOO_LARGE,
+ * MUON_ERR_UNSUPPORTED_DEVICE or MUON_ERR_CUDA. */
+muon_status_t fp8_mm_backward(const void* g, const void* x_f8, const void* w_f8, float x_s, float w_s, float grad_s,
+                              void* grad_x, void* grad_w, void* g_f8, int64_t M, int64_t N, int64_t K,
+                              void* workspace, size_t workspace_bytes, void* stream);
 
 /* Assigns each matrix of a bank to one of `world` ranks, for running the
  * step on several GPUs, one process per GPU, each updating only the matrices

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libmuon.so")
-SOURCES = ["muon_capi.cu", "elementwise.cu", "ns_gemm.cu", "noalloc.cu", "partition.cu", "adam.cu"]
+SOURCES = ["muon_capi.cu", "elementwise.cu", "ns_gemm.cu", "fp8.cu", "noalloc.cu", "partition.cu", "adam.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -17,13 +17,9 @@
 // normalise: X0 = bf16(Xraw * (1 / (sqrt(sum of the matrix's partials) +
 //   1e-7))), in place; the partials are summed in a fixed order by every
 //   block.
-// fp8_quantize: the operands of the FP8 scaled product, q = E4M3(bf16(x /
-//   s)) (page section "自定义FP8矩阵乘法实现": x.div(x_s).to(float8_e4m3fn)).
 // apply: after the last step, O = X in the stored orientation written
 //   (Newton-Schulz alone), or p <- p - lr * O for a Muon step with no
 //   iteration (otherwise the last update applies it).
-#include <cuda_fp8.h>
-
 #include "plan.h"
 
 namespace muon {
@@ -614,63 +610,6 @@ __global__ void __launch_bounds__(kEwThreads) apply_kernel(const __grid_constant
 cudaError_t launch_momentum_cast(const K1Params& P, int blocks, cudaStream_t stream) {
   void* args[] = {const_cast<K1Params*>(&P)};
   return launch_pdl(reinterpret_cast<const void*>(&momentum_cast_kernel), blocks, args, stream);
-}
-
-// ------------------------------------------------------------- FP8 operands
-// x / s rounded once to bfloat16: the quotient truncated to fp32 with its
-// last bit set when the division is inexact ("round to odd", Boldo and
-// Melquiond, "When double rounding is odd", 2005) rounds to bfloat16 (16
-// fewer bits) exactly as the exact quotient would.  The remainder
-// x - q s of a faithfully rounded quotient is representable, so the fused
-// multiply-add gives it exactly.
-__device__ __forceinline__ float div_to_bf16(float x, float s) {
-  const float q = __fdiv_rz(x, s);
-  const float r = fmaf(-q, s, x);
-  uint32_t b = __float_as_uint(q);
-  if (r != 0.0f && isfinite(q)) b |= 1u;
-  return __bfloat162float(__float2bfloat16_rn(__uint_as_float(b)));
-}
-
-// E4M3 ("fn", no infinities): round to nearest even; past the rounding range
-// of the largest finite value 448 (|v| > 464) the result is NaN, and so are
-// infinite and NaN inputs.
-__device__ __forceinline__ uint8_t to_e4m3(float v) {
-  if (!(fabsf(v) <= 464.0f)) return 0x7F;
-  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
-}
-
-__global__ void __launch_bounds__(kEwThreads) fp8_quantize_kernel(const __grid_constant__ Fp8QuantParams P) {
-  ptx_grid_dep_wait();
-  const int t = static_cast<long long>(blockIdx.x) >= P.blocks0 ? 1 : 0;
-  const long long b = static_cast<long long>(blockIdx.x) - (t ? P.blocks0 : 0);
-  const long long i0 = (b * kEwThreads + threadIdx.x) * 8;
-  const long long n = P.n[t];
-  if (i0 >= n) return;
-  const float s = P.scale[t];
-  const __nv_bfloat16* src = P.src[t];
-  uint8_t* dst = P.dst[t];
-  if (i0 + 8 <= n) {
-    // src 16-byte aligned and dst 8-byte aligned: bases are 16-byte aligned
-    const uint4 w = *reinterpret_cast<const uint4*>(src + i0);
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-    uint32_t lo = 0, hi = 0;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t a = to_e4m3(div_to_bf16(__uint_as_float(ws[k] << 16), s));
-      const uint32_t c = to_e4m3(div_to_bf16(__uint_as_float(ws[k] & 0xFFFF0000u), s));
-      const uint32_t pair = a | (c << 8);
-      if (k < 2) lo |= pair << (16 * k);
-      else hi |= pair << (16 * (k - 2));
-    }
-    *reinterpret_cast<uint2*>(dst + i0) = make_uint2(lo, hi);
-  } else {
-    for (long long i = i0; i < n; ++i) dst[i] = to_e4m3(div_to_bf16(__bfloat162float(src[i]), s));
-  }
-}
-
-cudaError_t launch_fp8_quantize(const Fp8QuantParams& P, int blocks, cudaStream_t stream) {
-  void* args[] = {const_cast<Fp8QuantParams*>(&P)};
-  return launch_pdl(reinterpret_cast<const void*>(&fp8_quantize_kernel), blocks, args, stream);
 }
 
 cudaError_t launch_apply(const ApplyParams& P, int blocks, cudaStream_t stream) {

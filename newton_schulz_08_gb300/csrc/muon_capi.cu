@@ -22,19 +22,26 @@
 #include <climits>
 #include <cmath>
 #include <cstring>
+#include <initializer_list>
+#include <list>
+#include <memory>
 #include <mutex>
 #include <vector>
 
 #include "../../include/muon.h"
 #include "plan.h"
+#include "ptx.cuh"
 
 namespace muon {
 
-cudaError_t launch_ns_gemm(int mode, int sym, const GemmParams& P, int num_sms, cudaStream_t stream);
+cudaError_t ns_gemm_pairs(int mode, int variant, int num_sms, int* pairs);
+cudaError_t launch_ns_gemm(int mode, int variant, const GemmParams& P, int pairs, cudaStream_t stream);
 cudaError_t launch_momentum_cast(const K1Params& P, int blocks, cudaStream_t stream);
 cudaError_t launch_normalise(const NormParams& P, int blocks, cudaStream_t stream);
 cudaError_t launch_apply(const ApplyParams& P, int blocks, cudaStream_t stream);
 cudaError_t launch_fp8_quantize(const Fp8QuantParams& P, int blocks, cudaStream_t stream);
+cudaError_t launch_fp8_transpose(const Fp8TParams& P, int blocks, cudaStream_t stream);
+cudaError_t launch_fp8_reduce(const Fp8ReduceParams& P, int blocks, cudaStream_t stream);
 
 namespace {
 
@@ -50,6 +57,7 @@ std::atomic<long long> g_wait_budget{4000000000LL};
 std::atomic<int> g_inject_stall{0};
 std::atomic<int> g_record_events{0};
 std::atomic<long long> g_wait_profile{0};  // device address of the counters, 0: off
+std::atomic<int> g_fail_encode{0};         // test hook: every tensor-map encode fails
 
 // Optional CUDA-event brackets around every launch (diagnostics).
 // kinds: 0 momentum_cast, 1 normalise, 2 gram, 3 poly, 4 update, 5 apply,
@@ -262,7 +270,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 bool encode_map(CUtensorMap* map, void* base, int cols, int rows, int count, int pitch, int box_cols,
                 int box_rows, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto enc = tensor_map_encoder();
-  if (!enc) return false;
+  if (!enc || g_fail_encode.load()) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
                         static_cast<cuuint64_t>(count)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch) * 2,
@@ -279,7 +287,7 @@ bool encode_map(CUtensorMap* map, void* base, int cols, int rows, int count, int
 bool encode_map_u8(CUtensorMap* map, void* base, long long cols, long long rows, long long pitch, int box_cols,
                    int box_rows) {
   auto enc = tensor_map_encoder();
-  if (!enc) return false;
+  if (!enc || g_fail_encode.load()) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), 1};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch), static_cast<cuuint64_t>(pitch) * static_cast<cuuint64_t>(rows)};
   cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
@@ -296,7 +304,7 @@ bool encode_map_u8(CUtensorMap* map, void* base, long long cols, long long rows,
 // multiple of 64 (a chunk never reaches past a row).
 bool encode_map4(CUtensorMap* map, void* base, int cols, int rows, int count, int pitch) {
   auto enc = tensor_map_encoder();
-  if (!enc || cols % 64 != 0) return false;
+  if (!enc || cols % 64 != 0 || g_fail_encode.load()) return false;
   cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols / 64),
                         static_cast<cuuint64_t>(count)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(pitch) * 2, 128,
@@ -314,14 +322,39 @@ int sym_tiles_per_mat(int m) {
   return tn * (tn + 1) / 2;
 }
 
-// ------------------------------------------------------------------ the run
-muon_status_t run(const std::vector<JobMat>& mats, const Plan& P, float lr, float mu, int nesterov,
-                  int ns_steps, int final_mode, char* ws, cudaStream_t stream, int sms) {
+// ------------------------------------------------------------- prepared call
+// Everything a call enqueues, computed before the first enqueue: launch
+// parameters with every tensor map encoded, grid sizes, and the order.  The
+// per-call scalars (lr, momentum, Nesterov flag) and the diagnostic knobs
+// are patched into a copy at enqueue time, so a prepared call depends only
+// on the device, the entry point, the pointers and shapes, ns_steps and the
+// workspace address.
+enum LaunchType { kLMomentum = 0, kLNorm, kLGemm, kLApply };
+
+struct LaunchRec {
+  int type;     // LaunchType
+  int ev_kind;  // kernel kind for the event brackets
+  int grid;     // blocks (elementwise passes) or CTA pairs (GEMMs)
+  int mode, variant;
+  int index;    // into the typed parameter vector
+};
+
+struct Prepared {
+  size_t ws_total = 0;
+  std::vector<K1Params> k1;
+  std::vector<NormParams> norm;
+  std::vector<GemmParams> gemm;
+  std::vector<ApplyParams> apply;
+  std::vector<LaunchRec> seq;
+};
+
+muon_status_t prepare(const std::vector<JobMat>& mats, const Plan& P, int ns_steps, int final_mode, char* ws,
+                      int sms, Prepared& Q) {
   const int N = static_cast<int>(mats.size());
-  int* status = reinterpret_cast<int*>(ws);
+  Q.ws_total = P.total;
   float* partials = reinterpret_cast<float*>(ws + P.parts_off);
   MatInfo* table = reinterpret_cast<MatInfo*>(ws + P.table_off);
-  if (cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess) return MUON_ERR_CUDA;
+  int* status = reinterpret_cast<int*>(ws);
 
   // momentum + cast (+ transpose) + partial norms
   for (int k0 = 0; k0 < N; k0 += kK1MaxMats) {
@@ -355,51 +388,41 @@ muon_status_t run(const std::vector<JobMat>& mats, const Plan& P, float lr, floa
     }
     kp.block_begin[n] = blocks;
     kp.n = n;
-    kp.mu = mu;
-    kp.nesterov = nesterov;
     kp.partials = partials;
     kp.table = table;
-    EventPair ev;
-    const bool rec = ev_begin(ev, 0, stream);
-    if (launch_momentum_cast(kp, blocks, stream) != cudaSuccess) return MUON_ERR_CUDA;
-    ev_end(ev, rec, stream);
+    Q.seq.push_back({kLMomentum, 0, blocks, 0, 0, static_cast<int>(Q.k1.size())});
+    Q.k1.push_back(kp);
   }
 
   // normalise
-  {
-    for (size_t c0 = 0; c0 < P.cls.size(); c0 += kMaxClasses) {
-      NormParams np;
-      std::memset(&np, 0, sizeof(np));
-      const int nc = static_cast<int>(std::min<size_t>(kMaxClasses, P.cls.size() - c0));
-      int blocks = 0;
-      for (int j = 0; j < nc; ++j) {
-        const ClassPlan& cp = P.cls[c0 + j];
-        NormClass& k = np.cls[j];
-        k.x = reinterpret_cast<__nv_bfloat16*>(ws + cp.x_off[0]);
-        k.count = cp.count;
-        k.m = cp.m;
-        k.n = cp.n;
-        k.ldx = cp.ldx;
-        k.mat_begin = cp.mat_begin;
-        k.rows_per_block = cp.norm_rpb;
-        k.blocks_per_mat = cp.norm_blocks;
-        k.block_begin = blocks;
-        blocks += cp.norm_blocks * cp.count;
-      }
-      np.n_classes = nc;
-      np.partials = partials;
-      np.table = table;
-      np.status = status;
-      EventPair ev;
-      const bool rec = ev_begin(ev, 1, stream);
-      if (launch_normalise(np, blocks, stream) != cudaSuccess) return MUON_ERR_CUDA;
-      ev_end(ev, rec, stream);
+  for (size_t c0 = 0; c0 < P.cls.size(); c0 += kMaxClasses) {
+    NormParams np;
+    std::memset(&np, 0, sizeof(np));
+    const int nc = static_cast<int>(std::min<size_t>(kMaxClasses, P.cls.size() - c0));
+    int blocks = 0;
+    for (int j = 0; j < nc; ++j) {
+      const ClassPlan& cp = P.cls[c0 + j];
+      NormClass& k = np.cls[j];
+      k.x = reinterpret_cast<__nv_bfloat16*>(ws + cp.x_off[0]);
+      k.count = cp.count;
+      k.m = cp.m;
+      k.n = cp.n;
+      k.ldx = cp.ldx;
+      k.mat_begin = cp.mat_begin;
+      k.rows_per_block = cp.norm_rpb;
+      k.blocks_per_mat = cp.norm_blocks;
+      k.block_begin = blocks;
+      blocks += cp.norm_blocks * cp.count;
     }
+    np.n_classes = nc;
+    np.partials = partials;
+    np.table = table;
+    np.status = status;
+    Q.seq.push_back({kLNorm, 1, blocks, 0, 0, static_cast<int>(Q.norm.size())});
+    Q.norm.push_back(np);
   }
 
   // Newton-Schulz steps
-  const long long budget = g_wait_budget.load();
-  const int stall = g_inject_stall.load();
   for (int t = 0; t < ns_steps; ++t) {
     const int src = t & 1, dst = src ^ 1;
     for (size_t c0 = 0; c0 < P.cls.size(); c0 += kMaxClasses) {
@@ -407,86 +430,83 @@ muon_status_t run(const std::vector<JobMat>& mats, const Plan& P, float lr, floa
       // Gram and polynomial: classes whose A is stored block-upper (m up to
       // kSymUpperMaxM) and the others go to separate kernel instantiations
       for (int mode = kGram; mode <= kUpdate; ++mode) {
-       for (int sym = 0; sym <= (mode == kUpdate ? 0 : 1); ++sym) {
-        GemmParams gp;
-        std::memset(&gp, 0, sizeof(gp));
-        int tiles = 0;
-        int ng = 0;
-        for (int j = 0; j < nc; ++j) {
-          const ClassPlan& cp = P.cls[c0 + j];
-          if (mode != kUpdate && (cp.m <= kSymUpperMaxM ? 1 : 0) != sym) continue;
-          GemmClass& g = gp.cls[ng++];
-          void* xs = ws + cp.x_off[src];
-          void* xd = ws + cp.x_off[dst];
-          void* A = ws + cp.a_off;
-          void* B = ws + cp.b_off;
-          bool ok = true;
-          // operands: A rows (box 64 x 128 per CTA), B rows or X columns, and
-          // the symmetric operand's stored blocks read transposed (64 x 64);
-          // epilogue: input and output boxes of one warp (64 x 32)
-          if (mode == kGram) {
-            ok = encode_map(&g.tmA, xs, cp.n, cp.m, cp.count, cp.ldx, kBK, kBM / 2) &&
-                 encode_map(&g.tmB, xs, cp.n, cp.m, cp.count, cp.ldx, kBK, kBN / 2) &&
-                 encode_map(&g.tmAux, A, cp.m, cp.m, cp.count, cp.lda, 64, kEpiRows) &&
-                 encode_map(&g.tmOut, A, cp.m, cp.m, cp.count, cp.lda, 64, kEpiRows) &&
-                 encode_map(&g.tmT, A, cp.m, cp.m, cp.count, cp.lda, 64, kBK);
-            g.K = cp.n;
-          } else if (mode == kPoly) {
-            ok = encode_map(&g.tmA, A, cp.m, cp.m, cp.count, cp.lda, kBK, kBM / 2) &&
-                 encode_map(&g.tmB, A, cp.m, cp.m, cp.count, cp.lda, kBK, kBN / 2) &&
-                 encode_map(&g.tmAux, A, cp.m, cp.m, cp.count, cp.lda, 64, kEpiRows) &&
-                 encode_map(&g.tmOut, B, cp.m, cp.m, cp.count, cp.lda, 64, kEpiRows) &&
-                 encode_map(&g.tmT, A, cp.m, cp.m, cp.count, cp.lda, 64, kBK);
-            g.K = cp.m;
-          } else {
-            ok = encode_map(&g.tmA, B, cp.m, cp.m, cp.count, cp.lda, kBK, kBM / 2) &&
-                 encode_map(&g.tmB, xs, cp.n, cp.m, cp.count, cp.ldx, 64, kBK) &&
-                 encode_map(&g.tmAux, xs, cp.n, cp.m, cp.count, cp.ldx, 64, kEpiRows) &&
-                 encode_map(&g.tmOut, xd, cp.n, cp.m, cp.count, cp.ldx, 64, kEpiRows) &&
-                 encode_map(&g.tmT, B, cp.m, cp.m, cp.count, cp.lda, 64, kBK);
-            g.K = cp.m;
+        for (int sym = 0; sym <= (mode == kUpdate ? 0 : 1); ++sym) {
+          GemmParams gp;
+          std::memset(&gp, 0, sizeof(gp));
+          int tiles = 0;
+          int ng = 0;
+          for (int j = 0; j < nc; ++j) {
+            const ClassPlan& cp = P.cls[c0 + j];
+            if (mode != kUpdate && (cp.m <= kSymUpperMaxM ? 1 : 0) != sym) continue;
+            GemmClass& g = gp.cls[ng++];
+            void* xs = ws + cp.x_off[src];
+            void* xd = ws + cp.x_off[dst];
+            void* A = ws + cp.a_off;
+            void* B = ws + cp.b_off;
+            bool ok = true;
+            // operands: A rows (box 64 x 128 per CTA), B rows or X columns, and
+            // the symmetric operand's stored blocks read transposed (64 x 64);
+            // epilogue: input and output boxes of one warp (64 x 32)
+            if (mode == kGram) {
+              ok = encode_map(&g.tmA, xs, cp.n, cp.m, cp.count, cp.ldx, kBK, kBM / 2) &&
+                   encode_map(&g.tmB, xs, cp.n, cp.m, cp.count, cp.ldx, kBK, kBN / 2) &&
+                   encode_map(&g.tmAux, A, cp.m, cp.m, cp.count, cp.lda, 64, kEpiRows) &&
+                   encode_map(&g.tmOut, A, cp.m, cp.m, cp.count, cp.lda, 64, kEpiRows) &&
+                   encode_map(&g.tmT, A, cp.m, cp.m, cp.count, cp.lda, 64, kBK);
+              g.K = cp.n;
+            } else if (mode == kPoly) {
+              ok = encode_map(&g.tmA, A, cp.m, cp.m, cp.count, cp.lda, kBK, kBM / 2) &&
+                   encode_map(&g.tmB, A, cp.m, cp.m, cp.count, cp.lda, kBK, kBN / 2) &&
+                   encode_map(&g.tmAux, A, cp.m, cp.m, cp.count, cp.lda, 64, kEpiRows) &&
+                   encode_map(&g.tmOut, B, cp.m, cp.m, cp.count, cp.lda, 64, kEpiRows) &&
+                   encode_map(&g.tmT, A, cp.m, cp.m, cp.count, cp.lda, 64, kBK);
+              g.K = cp.m;
+            } else {
+              ok = encode_map(&g.tmA, B, cp.m, cp.m, cp.count, cp.lda, kBK, kBM / 2) &&
+                   encode_map(&g.tmB, xs, cp.n, cp.m, cp.count, cp.ldx, 64, kBK) &&
+                   encode_map(&g.tmAux, xs, cp.n, cp.m, cp.count, cp.ldx, 64, kEpiRows) &&
+                   encode_map(&g.tmOut, xd, cp.n, cp.m, cp.count, cp.ldx, 64, kEpiRows) &&
+                   encode_map(&g.tmT, B, cp.m, cp.m, cp.count, cp.lda, 64, kBK);
+              g.K = cp.m;
+            }
+            if (!ok) return MUON_ERR_CUDA;
+            // poly: one-copy transposed reads of A where the width allows
+            g.t4 = mode == kPoly && sym && encode_map4(&g.tmT4, A, cp.m, cp.m, cp.count, cp.lda);
+            // mirrored entries of the Gram (wide A) and the polynomial (B)
+            if (mode != kUpdate && !encode_map(&g.tmMir, mode == kGram ? A : B, cp.m, cp.m, cp.count, cp.lda, 32,
+                                               64, CU_TENSOR_MAP_SWIZZLE_NONE))
+              return MUON_ERR_CUDA;
+            g.m = cp.m;
+            g.n = cp.n;
+            g.count = cp.count;
+            g.tiles_m = static_cast<int>(ceil_div(cp.m, kBM));
+            if (mode == kUpdate) {
+              g.tiles_n = static_cast<int>(ceil_div(cp.n, kBN));
+              g.tiles_per_mat = g.tiles_m * g.tiles_n;
+            } else {
+              g.tiles_n = static_cast<int>(ceil_div(cp.m, kBN));
+              g.tiles_per_mat = sym_tiles_per_mat(cp.m);
+            }
+            g.tile_begin = tiles;
+            g.mat_begin = cp.mat_begin;
+            tiles += g.tiles_per_mat * cp.count;
           }
-          if (!ok) return MUON_ERR_CUDA;
-          // poly: one-copy transposed reads of A where the width allows
-          g.t4 = mode == kPoly && sym && encode_map4(&g.tmT4, A, cp.m, cp.m, cp.count, cp.lda);
-          // mirrored entries of the Gram (wide A) and the polynomial (B)
-          if (mode != kUpdate && !encode_map(&g.tmMir, mode == kGram ? A : B, cp.m, cp.m, cp.count, cp.lda, 32, 64,
-                                             CU_TENSOR_MAP_SWIZZLE_NONE))
-            return MUON_ERR_CUDA;
-          g.m = cp.m;
-          g.n = cp.n;
-          g.count = cp.count;
-          g.tiles_m = static_cast<int>(ceil_div(cp.m, kBM));
-          if (mode == kUpdate) {
-            g.tiles_n = static_cast<int>(ceil_div(cp.n, kBN));
-            g.tiles_per_mat = g.tiles_m * g.tiles_n;
-          } else {
-            g.tiles_n = static_cast<int>(ceil_div(cp.m, kBN));
-            g.tiles_per_mat = sym_tiles_per_mat(cp.m);
-          }
-          g.tile_begin = tiles;
-          g.mat_begin = cp.mat_begin;
-          tiles += g.tiles_per_mat * cp.count;
+          if (ng == 0) continue;
+          gp.n_classes = ng;
+          gp.total_tiles = tiles;
+          gp.ca = kCoefA;
+          gp.cb = kCoefB;
+          gp.cc = kCoefC;
+          gp.status = status;
+          // the Muon step's last update applies p -= lr X' itself
+          gp.table = table;
+          gp.apply = mode == kUpdate && final_mode == kFinalParam && t == ns_steps - 1;
+          const int variant = mode == kUpdate ? gp.apply : sym;
+          int pairs = 0;
+          if (ns_gemm_pairs(mode, variant, sms, &pairs) != cudaSuccess) return MUON_ERR_CUDA;
+          Q.seq.push_back({kLGemm, gp.apply ? 6 : 2 + mode, pairs, mode, variant, static_cast<int>(Q.gemm.size())});
+          Q.gemm.push_back(gp);
         }
-        if (ng == 0) continue;
-        gp.n_classes = ng;
-        gp.total_tiles = tiles;
-        gp.ca = kCoefA;
-        gp.cb = kCoefB;
-        gp.cc = kCoefC;
-        gp.status = status;
-        gp.wait_budget = budget;
-        gp.inject_stall = stall;
-        gp.wait_profile = reinterpret_cast<long long*>(g_wait_profile.load());
-        // the Muon step's last update applies p -= lr X' itself
-        gp.table = table;
-        gp.lr = lr;
-        gp.apply = mode == kUpdate && final_mode == kFinalParam && t == ns_steps - 1;
-        EventPair ev;
-        const bool rec = ev_begin(ev, gp.apply ? 6 : 2 + mode, stream);
-        if (launch_ns_gemm(mode, sym, gp, sms, stream) != cudaSuccess) return MUON_ERR_CUDA;
-        ev_end(ev, rec, stream);
-       }
       }
     }
   }
@@ -516,14 +536,85 @@ muon_status_t run(const std::vector<JobMat>& mats, const Plan& P, float lr, floa
     }
     ap.n_classes = nc;
     ap.final_mode = final_mode;
-    ap.lr = lr;
     ap.table = table;
+    Q.seq.push_back({kLApply, 5, blocks, 0, 0, static_cast<int>(Q.apply.size())});
+    Q.apply.push_back(ap);
+  }
+  return MUON_OK;
+}
+
+// Enqueues a prepared call on `stream`: the status word is cleared, then
+// every kernel of the sequence is launched with the call's scalars.
+muon_status_t enqueue(const Prepared& Q, char* ws, float lr, float mu, int nesterov, cudaStream_t stream) {
+  if (cudaMemsetAsync(ws, 0, sizeof(int), stream) != cudaSuccess) return MUON_ERR_CUDA;
+  const long long budget = g_wait_budget.load();
+  const int stall = g_inject_stall.load();
+  long long* prof = reinterpret_cast<long long*>(g_wait_profile.load());
+  for (const LaunchRec& L : Q.seq) {
     EventPair ev;
-    const bool rec = ev_begin(ev, 5, stream);
-    if (launch_apply(ap, blocks, stream) != cudaSuccess) return MUON_ERR_CUDA;
+    const bool rec = ev_begin(ev, L.ev_kind, stream);
+    cudaError_t e = cudaSuccess;
+    if (L.type == kLMomentum) {
+      K1Params kp = Q.k1[L.index];
+      kp.mu = mu;
+      kp.nesterov = nesterov;
+      e = launch_momentum_cast(kp, L.grid, stream);
+    } else if (L.type == kLNorm) {
+      e = launch_normalise(Q.norm[L.index], L.grid, stream);
+    } else if (L.type == kLGemm) {
+      GemmParams gp = Q.gemm[L.index];
+      gp.lr = lr;
+      gp.wait_budget = budget;
+      gp.inject_stall = stall;
+      gp.wait_profile = prof;
+      e = launch_ns_gemm(L.mode, L.variant, gp, L.grid, stream);
+    } else {
+      ApplyParams ap = Q.apply[L.index];
+      ap.lr = lr;
+      e = launch_apply(ap, L.grid, stream);
+    }
+    if (e != cudaSuccess) return MUON_ERR_CUDA;
     ev_end(ev, rec, stream);
   }
   return MUON_OK;
+}
+
+// Prepared calls, most recently used first, keyed by the device, the entry
+// point and its pointer / shape arguments, ns_steps and the workspace
+// address (everything a prepared call depends on).  Host memory only.
+constexpr size_t kPlanCacheMax = 32;
+
+struct CacheEntry {
+  std::vector<uint64_t> key;
+  std::shared_ptr<const Prepared> plan;
+};
+
+std::mutex g_cache_mu;
+std::list<CacheEntry> g_cache;
+
+std::shared_ptr<const Prepared> cache_find(const std::vector<uint64_t>& key) {
+  if (g_fail_encode.load()) return nullptr;
+  std::lock_guard<std::mutex> lk(g_cache_mu);
+  for (auto it = g_cache.begin(); it != g_cache.end(); ++it) {
+    if (it->key == key) {
+      g_cache.splice(g_cache.begin(), g_cache, it);
+      return g_cache.front().plan;
+    }
+  }
+  return nullptr;
+}
+
+void cache_insert(std::vector<uint64_t> key, std::shared_ptr<const Prepared> plan) {
+  if (g_fail_encode.load()) return;
+  std::lock_guard<std::mutex> lk(g_cache_mu);
+  for (auto it = g_cache.begin(); it != g_cache.end(); ++it) {
+    if (it->key == key) {
+      g_cache.erase(it);
+      break;
+    }
+  }
+  g_cache.push_front({std::move(key), std::move(plan)});
+  while (g_cache.size() > kPlanCacheMax) g_cache.pop_back();
 }
 
 muon_status_t check_common(int ns_steps, void* ws, size_t ws_bytes, size_t need) {
@@ -534,9 +625,11 @@ muon_status_t check_common(int ns_steps, void* ws, size_t ws_bytes, size_t need)
   return MUON_OK;
 }
 
-muon_status_t plan_and_run(const std::vector<JobMat>& mats, std::vector<Range>& ranges, float lr,
-                           float mu, int nesterov, int ns_steps, int final_mode, void* ws,
-                           size_t ws_bytes, void* stream) {
+// Full checks and preparation of a call that was not in the cache; the
+// result is cached under `key` once everything has succeeded.
+muon_status_t plan_call(const std::vector<JobMat>& mats, std::vector<Range>& ranges, int ns_steps, int final_mode,
+                        void* ws, size_t ws_bytes, std::vector<uint64_t> key,
+                        std::shared_ptr<const Prepared>& out) {
   Plan P;
   if (!build_plan(mats, P)) return MUON_ERR_TOO_LARGE;
   muon_status_t s = check_common(ns_steps, ws, ws_bytes, P.total);
@@ -546,8 +639,28 @@ muon_status_t plan_and_run(const std::vector<JobMat>& mats, std::vector<Range>& 
   int sms = 0;
   s = current_device(sms);
   if (s != MUON_OK) return s;
-  return run(mats, P, lr, mu, nesterov, ns_steps, final_mode, static_cast<char*>(ws),
-             static_cast<cudaStream_t>(stream), sms);
+  auto Q = std::make_shared<Prepared>();
+  s = prepare(mats, P, ns_steps, final_mode, static_cast<char*>(ws), sms, *Q);
+  if (s != MUON_OK) return s;
+  out = Q;
+  if (!key.empty()) cache_insert(std::move(key), std::move(Q));
+  return MUON_OK;
+}
+
+// Cache key: device ordinal, entry point, ns_steps, workspace address, then
+// the entry point's own arguments.  Without a current device the key stays
+// empty and the call is neither looked up nor cached (the full checks then
+// report the call's own error first).
+void key_head(std::vector<uint64_t>& key, int entry, int ns_steps, const void* ws) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return;
+  }
+  key.push_back(static_cast<uint64_t>(dev));
+  key.push_back(static_cast<uint64_t>(entry));
+  key.push_back(static_cast<uint64_t>(static_cast<int64_t>(ns_steps)));
+  key.push_back(reinterpret_cast<uint64_t>(ws));
 }
 
 size_t plan_size(const std::vector<JobMat>& mats) {
@@ -591,6 +704,83 @@ bool collect_muon(const muon_mat_desc* mats, int n, std::vector<JobMat>& out,
   return true;
 }
 
+// 1 / s rounded to float for the quantise passes' fast quotient, or NaN
+// when it is not a normal float (the passes then divide exactly).
+float fast_inverse(float s) {
+  const float inv = static_cast<float>(1.0 / static_cast<double>(s));
+  return std::isnormal(inv) ? inv : NAN;
+}
+
+// FP8 backward: the contraction over the M rows (grad_w) is split in this
+// many slices when its output has few tiles, so that the product fills the
+// GPU; a pure function of the shapes (every slice non-empty).
+int fp8_bwd_ksplit(long long M, long long N, long long K) {
+  const long long tiles = ceil_div(N, kBN) * ceil_div(K, kBM);
+  const long long kblocks = ceil_div(M, 2 * kBK);
+  if (tiles >= 64) return 1;
+  long long s = std::min<long long>({4, ceil_div(72, tiles), kblocks});
+  const long long per = ceil_div(kblocks, s);
+  return static_cast<int>(ceil_div(kblocks, per));
+}
+
+struct Fp8BwdLayout {
+  size_t gT, xT, wT, part, total;
+  int ksplit;
+};
+
+Fp8BwdLayout fp8_bwd_layout(long long M, long long N, long long K) {
+  Fp8BwdLayout L;
+  L.ksplit = fp8_bwd_ksplit(M, N, K);
+  size_t off = 256;  // status word
+  L.gT = off;
+  off = align_up(off + static_cast<size_t>(N) * M, kAlign);
+  L.xT = off;
+  off = align_up(off + static_cast<size_t>(K) * M, kAlign);
+  L.wT = off;
+  off = align_up(off + static_cast<size_t>(K) * N, kAlign);
+  L.part = off;
+  if (L.ksplit > 1) off = align_up(off + sizeof(float) * L.ksplit * static_cast<size_t>(N) * K, kAlign);
+  L.total = off;
+  return L;
+}
+
+// 3-D fp32 map over `planes` row-major rows x cols planes (the partial sums
+// of a split product), 128-byte swizzle, box 32 x 32.
+bool encode_map_f32(CUtensorMap* map, void* base, long long cols, long long rows, int planes) {
+  auto enc = tensor_map_encoder();
+  if (!enc || g_fail_encode.load()) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(planes)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 4, static_cast<cuuint64_t>(cols) * 4 * static_cast<cuuint64_t>(rows)};
+  cuuint32_t box[3] = {32, static_cast<cuuint32_t>(kEpiRows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// One class of an FP8 product: out (rows x cols, bf16) = scale * (A . B^T)
+// with A rows x k and B cols x k one-byte codes, K-major.
+bool fp8_class(GemmClass& g, void* a, void* b, void* out, long long rows, long long cols, long long k, float scale,
+               int ksplit, void* part) {
+  if (!encode_map_u8(&g.tmA, a, k, rows, k, 2 * kBK, kBM / 2) || !encode_map_u8(&g.tmB, b, k, cols, k, 2 * kBK, kBN / 2) ||
+      !encode_map(&g.tmOut, out, static_cast<int>(cols), static_cast<int>(rows), 1, static_cast<int>(cols), 64,
+                  kEpiRows))
+    return false;
+  g.tmAux = g.tmT = g.tmT4 = g.tmMir = g.tmOut;
+  if (ksplit > 1 && !encode_map_f32(&g.tmAux, part, cols, rows, ksplit)) return false;
+  g.m = static_cast<int>(rows);
+  g.n = static_cast<int>(cols);
+  g.count = 1;
+  g.K = static_cast<int>(k);
+  g.tiles_m = static_cast<int>(ceil_div(rows, kBM));
+  g.tiles_n = static_cast<int>(ceil_div(cols, kBN));
+  g.ksplit = ksplit;
+  g.tiles_per_mat = g.tiles_m * g.tiles_n * ksplit;
+  g.scale = scale;
+  g.mat_begin = 0;
+  return true;
+}
+
 }  // namespace
 }  // namespace muon
 
@@ -619,12 +809,32 @@ muon_status_t muon_step(const muon_mat_desc* mats, int n_mats, float lr, float m
   if (n_mats == 0) return MUON_OK;
   if (n_mats < 0 || !mats) return MUON_ERR_INVALID_ARG;
   if (nesterov != 0 && nesterov != 1) return MUON_ERR_INVALID_ARG;
-  std::vector<JobMat> v;
-  std::vector<Range> ranges;
-  muon_status_t err;
-  if (!collect_muon(mats, n_mats, v, &ranges, err)) return err;
-  return plan_and_run(v, ranges, lr, momentum, nesterov, ns_steps, kFinalParam, workspace,
-                      workspace_bytes, stream);
+  if (ns_steps < 0) return MUON_ERR_INVALID_ARG;
+  std::vector<uint64_t> key;
+  key.reserve(4 + 6 * static_cast<size_t>(n_mats));
+  key_head(key, 0, ns_steps, workspace);
+  const bool keyed = !key.empty();
+  for (int i = 0; keyed && i < n_mats; ++i) {
+    const muon_mat_desc& d = mats[i];
+    key.push_back(reinterpret_cast<uint64_t>(d.param));
+    key.push_back(reinterpret_cast<uint64_t>(d.grad));
+    key.push_back(reinterpret_cast<uint64_t>(d.buf));
+    key.push_back(static_cast<uint64_t>(d.rows));
+    key.push_back(static_cast<uint64_t>(d.cols));
+    key.push_back((static_cast<uint64_t>(static_cast<uint32_t>(d.grad_dtype)) << 32) |
+                  static_cast<uint32_t>(d.reserved));
+  }
+  std::shared_ptr<const Prepared> Q = keyed ? cache_find(key) : nullptr;
+  if (!Q) {
+    std::vector<JobMat> v;
+    std::vector<Range> ranges;
+    muon_status_t err;
+    if (!collect_muon(mats, n_mats, v, &ranges, err)) return err;
+    err = plan_call(v, ranges, ns_steps, kFinalParam, workspace, workspace_bytes, std::move(key), Q);
+    if (err != MUON_OK) return err;
+  }
+  if (workspace_bytes < Q->ws_total) return MUON_ERR_WORKSPACE_TOO_SMALL;
+  return enqueue(*Q, static_cast<char*>(workspace), lr, momentum, nesterov, static_cast<cudaStream_t>(stream));
 }
 
 size_t ns5_workspace_size(int batch, int64_t rows, int64_t cols) {
@@ -642,21 +852,35 @@ muon_status_t ns5(const void* G, int g_dtype, void* O, int batch, int64_t rows, 
   muon_status_t s = check_shapes(rows, cols);
   if (s != MUON_OK) return s;
   if (!aligned16(G) || !aligned16(O)) return MUON_ERR_MISALIGNED;
-  const long long per = rows * cols;
-  const size_t gsz = g_dtype == MUON_F32 ? 4 : 2;
-  std::vector<JobMat> v(batch);
-  for (int i = 0; i < batch; ++i) {
-    v[i].g = static_cast<const char*>(G) + gsz * per * i;
-    v[i].g_f32 = g_dtype == MUON_F32;
-    v[i].buf = nullptr;
-    v[i].out = static_cast<char*>(O) + 2 * per * i;
-    v[i].R = rows;
-    v[i].C = cols;
+  if (ns_steps < 0) return MUON_ERR_INVALID_ARG;
+  std::vector<uint64_t> key;
+  key_head(key, 1, ns_steps, workspace);
+  const bool keyed = !key.empty();
+  if (keyed)
+    for (uint64_t v : {reinterpret_cast<uint64_t>(G), static_cast<uint64_t>(g_dtype), reinterpret_cast<uint64_t>(O),
+                       static_cast<uint64_t>(batch), static_cast<uint64_t>(rows), static_cast<uint64_t>(cols)})
+      key.push_back(v);
+  std::shared_ptr<const Prepared> Q = keyed ? cache_find(key) : nullptr;
+  if (!Q) {
+    const long long per = rows * cols;
+    const size_t gsz = g_dtype == MUON_F32 ? 4 : 2;
+    std::vector<JobMat> v(batch);
+    for (int i = 0; i < batch; ++i) {
+      v[i].g = static_cast<const char*>(G) + gsz * per * i;
+      v[i].g_f32 = g_dtype == MUON_F32;
+      v[i].buf = nullptr;
+      v[i].out = static_cast<char*>(O) + 2 * per * i;
+      v[i].R = rows;
+      v[i].C = cols;
+    }
+    std::vector<Range> ranges = {
+        {reinterpret_cast<uintptr_t>(G), reinterpret_cast<uintptr_t>(G) + gsz * per * batch, false},
+        {reinterpret_cast<uintptr_t>(O), reinterpret_cast<uintptr_t>(O) + 2 * per * batch, true}};
+    s = plan_call(v, ranges, ns_steps, kFinalOut, workspace, workspace_bytes, std::move(key), Q);
+    if (s != MUON_OK) return s;
   }
-  std::vector<Range> ranges = {
-      {reinterpret_cast<uintptr_t>(G), reinterpret_cast<uintptr_t>(G) + gsz * per * batch, false},
-      {reinterpret_cast<uintptr_t>(O), reinterpret_cast<uintptr_t>(O) + 2 * per * batch, true}};
-  return plan_and_run(v, ranges, 0.0f, 0.0f, 0, ns_steps, kFinalOut, workspace, workspace_bytes, stream);
+  if (workspace_bytes < Q->ws_total) return MUON_ERR_WORKSPACE_TOO_SMALL;
+  return enqueue(*Q, static_cast<char*>(workspace), 0.0f, 0.0f, 0, static_cast<cudaStream_t>(stream));
 }
 
 size_t ns5_bank_workspace_size(const int64_t* rows, const int64_t* cols, int n_mats) {
@@ -675,25 +899,43 @@ muon_status_t ns5_bank(const void* const* G, const int32_t* g_dtype, void* const
                        size_t workspace_bytes, void* stream) {
   if (n_mats == 0) return MUON_OK;
   if (n_mats < 0 || !G || !g_dtype || !O || !rows || !cols) return MUON_ERR_INVALID_ARG;
-  std::vector<JobMat> v(n_mats);
-  std::vector<Range> ranges;
-  for (int i = 0; i < n_mats; ++i) {
-    if (!G[i] || !O[i] || (g_dtype[i] != MUON_BF16 && g_dtype[i] != MUON_F32)) return MUON_ERR_INVALID_ARG;
-    muon_status_t s = check_shapes(rows[i], cols[i]);
-    if (s != MUON_OK) return s;
-    if (!aligned16(G[i]) || !aligned16(O[i])) return MUON_ERR_MISALIGNED;
-    const uintptr_t e = static_cast<uintptr_t>(rows[i] * cols[i]);
-    v[i].g = G[i];
-    v[i].g_f32 = g_dtype[i] == MUON_F32;
-    v[i].buf = nullptr;
-    v[i].out = O[i];
-    v[i].R = rows[i];
-    v[i].C = cols[i];
-    ranges.push_back({reinterpret_cast<uintptr_t>(G[i]),
-                      reinterpret_cast<uintptr_t>(G[i]) + (v[i].g_f32 ? 4 : 2) * e, false});
-    ranges.push_back({reinterpret_cast<uintptr_t>(O[i]), reinterpret_cast<uintptr_t>(O[i]) + 2 * e, true});
+  if (ns_steps < 0) return MUON_ERR_INVALID_ARG;
+  std::vector<uint64_t> key;
+  key.reserve(4 + 5 * static_cast<size_t>(n_mats));
+  key_head(key, 2, ns_steps, workspace);
+  const bool keyed = !key.empty();
+  for (int i = 0; keyed && i < n_mats; ++i) {
+    key.push_back(reinterpret_cast<uint64_t>(G[i]));
+    key.push_back(static_cast<uint64_t>(static_cast<uint32_t>(g_dtype[i])));
+    key.push_back(reinterpret_cast<uint64_t>(O[i]));
+    key.push_back(static_cast<uint64_t>(rows[i]));
+    key.push_back(static_cast<uint64_t>(cols[i]));
   }
-  return plan_and_run(v, ranges, 0.0f, 0.0f, 0, ns_steps, kFinalOut, workspace, workspace_bytes, stream);
+  std::shared_ptr<const Prepared> Q = keyed ? cache_find(key) : nullptr;
+  if (!Q) {
+    std::vector<JobMat> v(n_mats);
+    std::vector<Range> ranges;
+    for (int i = 0; i < n_mats; ++i) {
+      if (!G[i] || !O[i] || (g_dtype[i] != MUON_BF16 && g_dtype[i] != MUON_F32)) return MUON_ERR_INVALID_ARG;
+      muon_status_t s = check_shapes(rows[i], cols[i]);
+      if (s != MUON_OK) return s;
+      if (!aligned16(G[i]) || !aligned16(O[i])) return MUON_ERR_MISALIGNED;
+      const uintptr_t e = static_cast<uintptr_t>(rows[i] * cols[i]);
+      v[i].g = G[i];
+      v[i].g_f32 = g_dtype[i] == MUON_F32;
+      v[i].buf = nullptr;
+      v[i].out = O[i];
+      v[i].R = rows[i];
+      v[i].C = cols[i];
+      ranges.push_back({reinterpret_cast<uintptr_t>(G[i]),
+                        reinterpret_cast<uintptr_t>(G[i]) + (v[i].g_f32 ? 4 : 2) * e, false});
+      ranges.push_back({reinterpret_cast<uintptr_t>(O[i]), reinterpret_cast<uintptr_t>(O[i]) + 2 * e, true});
+    }
+    muon_status_t s = plan_call(v, ranges, ns_steps, kFinalOut, workspace, workspace_bytes, std::move(key), Q);
+    if (s != MUON_OK) return s;
+  }
+  if (workspace_bytes < Q->ws_total) return MUON_ERR_WORKSPACE_TOO_SMALL;
+  return enqueue(*Q, static_cast<char*>(workspace), 0.0f, 0.0f, 0, static_cast<cudaStream_t>(stream));
 }
 
 muon_status_t muon_device_status(const void* workspace, void* stream) {
@@ -763,7 +1005,16 @@ int muon_set_debug(const char* key, long long value) {
     g_record_events.store(value ? 1 : 0);
     return 0;
   }
+  if (!std::strcmp(key, "fail_tensor_map_encode")) {
+    g_fail_encode.store(value ? 1 : 0);
+    return 0;
+  }
   return -1;
+}
+
+void muon_plan_cache_clear(void) {
+  std::lock_guard<std::mutex> lk(g_cache_mu);
+  g_cache.clear();
 }
 
 int muon_kernel_times(double* ms, int* launches, int n_kinds) {
@@ -818,8 +1069,22 @@ muon_status_t fp8_mm(const void* x, const void* w, float x_s, float w_s, void* o
   int sms = 0;
   muon_status_t s = current_device(sms);
   if (s != MUON_OK) return s;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(workspace, 0, 256, st) != cudaSuccess) return MUON_ERR_CUDA;
+  // everything the launches take is prepared before the first enqueue
+  GemmParams gp;
+  std::memset(&gp, 0, sizeof(gp));
+  // the maps other than A, B and out are not read by the FP8 product (only
+  // prefetched)
+  if (!fp8_class(gp.cls[0], x_f8, w_f8, out, M, N, K,
+                 static_cast<float>(static_cast<double>(x_s) * static_cast<double>(w_s)), 1, nullptr))
+    return MUON_ERR_CUDA;
+  gp.n_classes = 1;
+  gp.total_tiles = static_cast<int>(tm * tn);
+  gp.idesc_f8 = ptx::idesc_f8(kBM, kBN, ptx::kFmtE4M3, ptx::kFmtE4M3);
+  gp.status = static_cast<int*>(workspace);
+  gp.wait_budget = g_wait_budget.load();
+  gp.inject_stall = g_inject_stall.load();
+  int pairs = 0;
+  if (ns_gemm_pairs(kFp8, 0, sms, &pairs) != cudaSuccess) return MUON_ERR_CUDA;
 
   Fp8QuantParams q;
   std::memset(&q, 0, sizeof(q));
@@ -831,38 +1096,141 @@ muon_status_t fp8_mm(const void* x, const void* w, float x_s, float w_s, void* o
   q.n[1] = N * K;
   q.scale[0] = x_s;
   q.scale[1] = w_s;
+  q.inv_scale[0] = fast_inverse(x_s);
+  q.inv_scale[1] = fast_inverse(w_s);
   q.blocks0 = ceil_div(M * K, kQuantPerBlock);
   const long long qblocks = q.blocks0 + ceil_div(N * K, kQuantPerBlock);
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, 256, st) != cudaSuccess) return MUON_ERR_CUDA;
   EventPair evq;
   const bool recq = ev_begin(evq, 7, st);
   if (launch_fp8_quantize(q, static_cast<int>(qblocks), st) != cudaSuccess) return MUON_ERR_CUDA;
   ev_end(evq, recq, st);
+  EventPair evg;
+  const bool recg = ev_begin(evg, 8, st);
+  if (launch_ns_gemm(kFp8, 0, gp, pairs, st) != cudaSuccess) return MUON_ERR_CUDA;
+  ev_end(evg, recg, st);
+  return MUON_OK;
+}
+
+size_t fp8_mm_backward_workspace_size(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || K < 0 || M % 16 || N % 16 || K % 16) return 0;
+  if (M > INT_MAX || N > INT_MAX || K > INT_MAX) return 0;
+  if (M == 0 || N == 0 || K == 0) return 256;
+  return fp8_bwd_layout(M, N, K).total;
+}
+
+// Backward of the FP8 scaled product (page section "自定义FP8矩阵乘法实现",
+// "反向传播优化"): g_f8 = E5M2(bf16(g / grad_s)), grad_x = bf16(grad_s w_s
+// (g_f8 . w_f8)), grad_w = bf16(grad_s x_s (g_f8^T . x_f8)), fp32 accumulation.
+muon_status_t fp8_mm_backward(const void* g, const void* x_f8, const void* w_f8, float x_s, float w_s, float grad_s,
+                              void* grad_x, void* grad_w, void* g_f8, int64_t M, int64_t N, int64_t K,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  if (M < 0 || N < 0 || K < 0) return MUON_ERR_INVALID_ARG;
+  if (M % 16 || N % 16 || K % 16) return MUON_ERR_INVALID_ARG;
+  if (!g || !x_f8 || !w_f8 || !grad_x || !grad_w || !g_f8 || !workspace) return MUON_ERR_INVALID_ARG;
+  for (float v : {x_s, w_s, grad_s})
+    if (!(std::isfinite(v) && v > 0.0f)) return MUON_ERR_INVALID_ARG;
+  if (M > INT_MAX || N > INT_MAX || K > INT_MAX) return MUON_ERR_TOO_LARGE;
+  if (M * K > (1LL << 40) || N * K > (1LL << 40) || M * N > (1LL << 40)) return MUON_ERR_TOO_LARGE;
+  if (ceil_div(M, kBM) * ceil_div(K, kBN) + 4 * ceil_div(N, kBM) * ceil_div(K, kBN) > (1LL << 24))
+    return MUON_ERR_TOO_LARGE;
+  for (const void* p : std::initializer_list<const void*>{g, x_f8, w_f8, grad_x, grad_w, g_f8})
+    if (!aligned16(p)) return MUON_ERR_MISALIGNED;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return MUON_ERR_MISALIGNED;
+  const bool empty = M == 0 || N == 0 || K == 0;
+  const Fp8BwdLayout L = empty ? Fp8BwdLayout{256, 256, 256, 256, 256, 1} : fp8_bwd_layout(M, N, K);
+  if (workspace_bytes < L.total) return MUON_ERR_WORKSPACE_TOO_SMALL;
+  auto at = [](const void* p) { return reinterpret_cast<uintptr_t>(p); };
+  const uintptr_t mn = static_cast<uintptr_t>(M * N), mk = static_cast<uintptr_t>(M * K),
+                  nk = static_cast<uintptr_t>(N * K);
+  std::vector<Range> ranges = {{at(g), at(g) + 2 * mn, false},           {at(x_f8), at(x_f8) + mk, false},
+                               {at(w_f8), at(w_f8) + nk, false},         {at(grad_x), at(grad_x) + 2 * mk, true},
+                               {at(grad_w), at(grad_w) + 2 * nk, true},  {at(g_f8), at(g_f8) + mn, true},
+                               {at(workspace), at(workspace) + L.total, true}};
+  if (ranges_overlap(ranges)) return MUON_ERR_ALIASING;
+  int sms = 0;
+  muon_status_t s = current_device(sms);
+  if (s != MUON_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (empty) {
+    // an empty contraction: the non-empty gradient is zero
+    if (cudaMemsetAsync(workspace, 0, 256, st) != cudaSuccess) return MUON_ERR_CUDA;
+    if (mk && cudaMemsetAsync(grad_x, 0, 2 * mk, st) != cudaSuccess) return MUON_ERR_CUDA;
+    if (nk && cudaMemsetAsync(grad_w, 0, 2 * nk, st) != cudaSuccess) return MUON_ERR_CUDA;
+    return MUON_OK;
+  }
+  char* ws = static_cast<char*>(workspace);
+  uint8_t* gT = reinterpret_cast<uint8_t*>(ws + L.gT);
+  uint8_t* xT = reinterpret_cast<uint8_t*>(ws + L.xT);
+  uint8_t* wT = reinterpret_cast<uint8_t*>(ws + L.wT);
+  float* part = reinterpret_cast<float*>(ws + L.part);
+
+  // everything the launches take is prepared before the first enqueue
+  Fp8TParams tp;
+  std::memset(&tp, 0, sizeof(tp));
+  int tblocks = 0;
+  auto job = [&](int j, const void* src, uint8_t* dst, uint8_t* dst_t, long long rows, long long cols, int quant) {
+    Fp8TJob& J = tp.job[j];
+    J.src = src;
+    J.dst = dst;
+    J.dst_t = dst_t;
+    J.rows = static_cast<int>(rows);
+    J.cols = static_cast<int>(cols);
+    J.quant = quant;
+    J.scale = grad_s;
+    J.inv_scale = fast_inverse(grad_s);
+    J.tiles_c = static_cast<int>(ceil_div(cols, kFp8Tile));
+    J.tile_begin = tblocks;
+    tblocks += static_cast<int>(ceil_div(rows, kFp8Tile) * J.tiles_c);
+  };
+  job(0, g, static_cast<uint8_t*>(g_f8), gT, M, N, 1);
+  job(1, x_f8, nullptr, xT, M, K, 0);
+  job(2, w_f8, nullptr, wT, N, K, 0);
+  tp.n_jobs = 3;
 
   GemmParams gp;
   std::memset(&gp, 0, sizeof(gp));
-  GemmClass& g = gp.cls[0];
-  if (!encode_map_u8(&g.tmA, x_f8, K, M, K, 2 * kBK, kBM / 2) || !encode_map_u8(&g.tmB, w_f8, K, N, K, 2 * kBK, kBN / 2) ||
-      !encode_map(&g.tmOut, out, static_cast<int>(N), static_cast<int>(M), 1, static_cast<int>(N), 64, kEpiRows))
+  // class 0, grad_w (N x K, contraction over M, the long tiles first);
+  // class 1, grad_x (M x K, contraction over N)
+  const float sw = static_cast<float>(static_cast<double>(grad_s) * static_cast<double>(x_s));
+  const float sx = static_cast<float>(static_cast<double>(grad_s) * static_cast<double>(w_s));
+  if (!fp8_class(gp.cls[0], gT, xT, grad_w, N, K, M, sw, L.ksplit, part) ||
+      !fp8_class(gp.cls[1], g_f8, wT, grad_x, M, K, N, sx, 1, nullptr))
     return MUON_ERR_CUDA;
-  // the other maps are not read by the FP8 product (only prefetched)
-  g.tmAux = g.tmT = g.tmT4 = g.tmMir = g.tmOut;
-  g.m = static_cast<int>(M);
-  g.n = static_cast<int>(N);
-  g.count = 1;
-  g.K = static_cast<int>(K);
-  g.tiles_m = static_cast<int>(tm);
-  g.tiles_n = static_cast<int>(tn);
-  g.tiles_per_mat = static_cast<int>(tm * tn);
-  gp.n_classes = 1;
-  gp.total_tiles = static_cast<int>(tm * tn);
-  gp.cc = static_cast<float>(static_cast<double>(x_s) * static_cast<double>(w_s));
+  gp.cls[0].tile_begin = 0;
+  gp.cls[1].tile_begin = gp.cls[0].tiles_per_mat;
+  gp.n_classes = 2;
+  gp.total_tiles = gp.cls[0].tiles_per_mat + gp.cls[1].tiles_per_mat;
+  gp.idesc_f8 = ptx::idesc_f8(kBM, kBN, ptx::kFmtE5M2, ptx::kFmtE4M3);
   gp.status = static_cast<int*>(workspace);
   gp.wait_budget = g_wait_budget.load();
   gp.inject_stall = g_inject_stall.load();
-  EventPair evg;
-  const bool recg = ev_begin(evg, 8, st);
-  if (launch_ns_gemm(kFp8, 0, gp, sms, st) != cudaSuccess) return MUON_ERR_CUDA;
-  ev_end(evg, recg, st);
+  int pairs = 0;
+  if (ns_gemm_pairs(kFp8, 0, sms, &pairs) != cudaSuccess) return MUON_ERR_CUDA;
+
+  Fp8ReduceParams rp;
+  rp.part = part;
+  rp.out = static_cast<__nv_bfloat16*>(grad_w);
+  rp.n = N * K;
+  rp.splits = L.ksplit;
+  rp.scale = sw;
+  const int rblocks = static_cast<int>(ceil_div(N * K, 4 * 256));
+
+  if (cudaMemsetAsync(workspace, 0, 256, st) != cudaSuccess) return MUON_ERR_CUDA;
+  EventPair ev;
+  bool rec = ev_begin(ev, 9, st);
+  if (launch_fp8_transpose(tp, tblocks, st) != cudaSuccess) return MUON_ERR_CUDA;
+  ev_end(ev, rec, st);
+  rec = ev_begin(ev, 10, st);
+  if (launch_ns_gemm(kFp8, 0, gp, pairs, st) != cudaSuccess) return MUON_ERR_CUDA;
+  ev_end(ev, rec, st);
+  if (L.ksplit > 1) {
+    rec = ev_begin(ev, 11, st);
+    if (launch_fp8_reduce(rp, rblocks, st) != cudaSuccess) return MUON_ERR_CUDA;
+    ev_end(ev, rec, st);
+  }
   return MUON_OK;
 }
 

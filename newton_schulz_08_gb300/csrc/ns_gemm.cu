@@ -55,6 +55,8 @@
 // 128 x 256 tiles.  Every barrier wait is bounded; on expiry the CTA raises
 // the timeout bit of the device status word, lets its copies and MMAs
 // drain, frees TMEM and returns.
+#include <mutex>
+
 #include "plan.h"
 #include "ptx.cuh"
 
@@ -64,6 +66,7 @@ namespace {
 
 struct Tile {
   int cls, idx, I, J;
+  int split;  // kFp8: slice of the contraction (0 when it is not split)
 };
 
 template <int MODE>
@@ -77,7 +80,14 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& P, int t) {
   r.cls = c;
   r.idx = local / C.tiles_per_mat;
   int q = local - r.idx * C.tiles_per_mat;
-  if (MODE == kUpdate || MODE == kFp8) {
+  r.split = 0;
+  if (MODE == kFp8) {
+    const int mn = C.tiles_m * C.tiles_n;
+    r.split = q / mn;
+    q -= r.split * mn;
+    r.I = q % C.tiles_m;
+    r.J = q / C.tiles_m;
+  } else if (MODE == kUpdate) {
     r.I = q % C.tiles_m;
     r.J = q / C.tiles_m;
   } else {
@@ -95,6 +105,21 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& P, int t) {
     r.J = J;
   }
   return r;
+}
+
+// K blocks [*kb0, *kb1) of a tile: the whole contraction, or the tile's
+// slice of it when the class splits it (kFp8)
+template <int MODE>
+__device__ __forceinline__ void k_range(const GemmClass& C, const Tile& tl, int kkb, int* kb0, int* kb1) {
+  const int kblocks = (C.K + kkb - 1) / kkb;
+  if (MODE == kFp8 && C.ksplit > 1) {
+    const int per = (kblocks + C.ksplit - 1) / C.ksplit;
+    *kb0 = tl.split * per;
+    *kb1 = min(kblocks, *kb0 + per);
+  } else {
+    *kb0 = 0;
+    *kb1 = kblocks;
+  }
 }
 
 __device__ __forceinline__ void raise_timeout(const GemmParams& P, volatile int* abort) {
@@ -201,8 +226,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       for (int t = pair; ok && t < P.total_tiles; t += npairs) {
         const Tile tl = decode_tile<MODE>(P, t);
         const GemmClass& C = P.cls[tl.cls];
-        const int kblocks = (C.K + kKB - 1) / kKB;
-        for (int kb = 0; kb < kblocks; ++kb) {
+        int kb0, kb1;
+        k_range<MODE>(C, tl, kKB, &kb0, &kb1);
+        for (int kb = kb0; kb < kb1; ++kb) {
           const long long w0 = prof ? clock64() : 0;
           if (!ptx::mbar_wait(ptx::smem_addr(&empty[stage]), phase ^ 1, budget, abort)) {
             raise_timeout(P, abort);
@@ -268,7 +294,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       for (int t = pair; ok && t < P.total_tiles; t += npairs, ++it) {
         const Tile tl = decode_tile<MODE>(P, t);
         const GemmClass& C = P.cls[tl.cls];
-        const int kblocks = (C.K + kKB - 1) / kKB;
+        int kb0, kb1;
+        k_range<MODE>(C, tl, kKB, &kb0, &kb1);
         const int acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
         const long long w1 = prof ? clock64() : 0;
@@ -279,7 +306,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         if (prof) prof[kWpMmaTempty] += clock64() - w1;
         ptx::tc_fence_after();
         const uint32_t d = tmem_base + acc * kBN;
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           const long long w2 = prof ? clock64() : 0;
           if (!ptx::mbar_wait(ptx::smem_addr(&full[stage]), phase, budget, abort)) {
             raise_timeout(P, abort);
@@ -300,10 +327,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
                                         : ptx::sdesc_sw128(sa + k * 32, 16, 1024);
             const uint64_t bdesc = b_mn ? ptx::sdesc_sw128(sb + k * 2048, 64 * kBK * 2, 1024)
                                         : ptx::sdesc_sw128(sb + k * 32, 16, 1024);
+            const uint32_t accum = (kb != kb0 || k != 0) ? 1u : 0u;
             if (MODE == kFp8)
-              ptx::mma_f8_pair(d, adesc, bdesc, ptx::idesc_e4m3(kBM, kBN), (kb | k) != 0 ? 1u : 0u);
+              ptx::mma_f8_pair(d, adesc, bdesc, P.idesc_f8, accum);
             else
-              ptx::mma_bf16_pair(d, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
+              ptx::mma_bf16_pair(d, adesc, bdesc, idesc, accum);
           }
           ptx::mma_commit_pair_mc(ptx::smem_addr(&empty[stage]), 0x3);
           if (++stage == kSt) {
@@ -471,6 +499,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         // staging box: the tile's 64-column box, or (Gram) the warp's one box
         const int sbx = kNoAux ? colhalf : (c0 >> 6);
         const uint32_t rowa = stg_a + sbx * ((kBM / 2) * 128) + row_local * 128;
+        if (MODE == kFp8 && C.ksplit > 1) {
+          // a slice of a split contraction: the fp32 partial sums of these
+          // 32 columns (128 bytes per row) fill the warp's 32 x 128-byte
+          // slot as one fp32 box, stored to the slice's plane of the
+          // partial-sum array once the previous chunk's box has been read
+          if (ch > 0) {
+            if (lane == 0) ptx::bulk_wait_read0();
+            __syncwarp();
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            ptx::sts128(rowa + ((j ^ (row_local & 7)) << 4), r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+          ptx::fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_3d(&C.tmAux, stg_a + colhalf * ((kBM / 2) * 128) + my_rows, tl.J * kBN + c0,
+                              tl.I * kBM + rowoff + q * kEpiRows, tl.split);
+            ptx::bulk_commit();
+          }
+          if (ch == 3) {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive_cluster(tempty_leader[acc]);
+          }
+          continue;
+        }
         if (kNoAux && ch == 2) {
           // the warp's box still holds its first half until the store has read it
           if (lane == 0) ptx::bulk_wait_read0();
@@ -487,7 +541,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
             // Gram: the product; FP8: the product times x_s w_s
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-              v[e] = MODE == kFp8 ? P.cc * __uint_as_float(r[8 * jj + e]) : __uint_as_float(r[8 * jj + e]);
+              v[e] = MODE == kFp8 ? C.scale * __uint_as_float(r[8 * jj + e]) : __uint_as_float(r[8 * jj + e]);
           } else {
             uint32_t x[4];
             ptx::lds128(addr, x[0], x[1], x[2], x[3]);
@@ -614,54 +668,93 @@ template __global__ void ns_gemm_kernel<kUpdate, 0, 1>(const __grid_constant__ G
 template __global__ void ns_gemm_kernel<kFp8, 0, 0>(const __grid_constant__ GemmParams P);
 
 // ------------------------------------------------------------------ launcher
-// Clusters of two CTAs (one pair per cluster), persistent: as many pairs as
-// can be resident at once, at most one per tile.
-cudaError_t launch_ns_gemm(int mode, int sym, const GemmParams& P, int num_sms, cudaStream_t stream) {
-  // Gram / polynomial: 1 = A stored block-upper; update: 1 = with the
-  // parameter update
-  const int variant = mode == kUpdate ? (P.apply ? 1 : 0) : mode == kFp8 ? 0 : (sym ? 1 : 0);
-  const void* fn =
-      mode == kGram ? (variant ? reinterpret_cast<const void*>(&ns_gemm_kernel<kGram, 1, 0>)
-                           : reinterpret_cast<const void*>(&ns_gemm_kernel<kGram, 0, 0>))
-      : mode == kPoly ? (variant ? reinterpret_cast<const void*>(&ns_gemm_kernel<kPoly, 1, 0>)
-                             : reinterpret_cast<const void*>(&ns_gemm_kernel<kPoly, 0, 0>))
-      : mode == kUpdate ? (variant ? reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate, 0, 1>)
-                                   : reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate, 0, 0>))
-                        : reinterpret_cast<const void*>(&ns_gemm_kernel<kFp8, 0, 0>);
-  const int slot = mode * 2 + variant;
-  const int smem = mode == kGram   ? GemmShape<kGram>::smem
-                   : mode == kPoly ? GemmShape<kPoly>::smem
-                   : mode == kUpdate ? GemmShape<kUpdate>::smem
-                                     : GemmShape<kFp8>::smem;
-  static int max_pairs[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  cudaError_t e = cudaSuccess;
-  if (max_pairs[slot] <= 0) {
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
+namespace {
+
+// The kernel instantiation of a (mode, variant) and its shared memory.
+// Variant: Gram / polynomial 1 = A stored block-upper; update 1 = with the
+// parameter update; FP8 0.
+const void* gemm_fn(int mode, int variant, int* smem) {
+  switch (mode) {
+    case kGram:
+      *smem = GemmShape<kGram>::smem;
+      return variant ? reinterpret_cast<const void*>(&ns_gemm_kernel<kGram, 1, 0>)
+                     : reinterpret_cast<const void*>(&ns_gemm_kernel<kGram, 0, 0>);
+    case kPoly:
+      *smem = GemmShape<kPoly>::smem;
+      return variant ? reinterpret_cast<const void*>(&ns_gemm_kernel<kPoly, 1, 0>)
+                     : reinterpret_cast<const void*>(&ns_gemm_kernel<kPoly, 0, 0>);
+    case kUpdate:
+      *smem = GemmShape<kUpdate>::smem;
+      return variant ? reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate, 0, 1>)
+                     : reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate, 0, 0>);
+    default:
+      *smem = GemmShape<kFp8>::smem;
+      return reinterpret_cast<const void*>(&ns_gemm_kernel<kFp8, 0, 0>);
   }
-  cudaLaunchAttribute attr[2];
+}
+
+void gemm_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[2], int smem, cudaStream_t stream) {
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
+  cfg = {};
   cfg.blockDim = dim3(kGemmThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (max_pairs[slot] <= 0) {
-    cfg.gridDim = dim3(num_sms);
-    int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+}
+
+constexpr int kMaxGemmDevices = 64;
+constexpr int kGemmSlots = 8;  // mode * 2 + variant
+std::mutex g_pairs_mu;
+int g_max_pairs[kMaxGemmDevices][kGemmSlots] = {};
+
+}  // namespace
+
+// CTA pairs of a (mode, variant) kernel that can be resident at once on the
+// current device, at most num_sms / 2.  The first query per device and
+// kernel also raises the kernel's dynamic shared-memory limit there; both
+// are kept per device.  Enqueues nothing.
+cudaError_t ns_gemm_pairs(int mode, int variant, int num_sms, int* pairs) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxGemmDevices) return cudaErrorInvalidDevice;
+  const int slot = mode * 2 + variant;
+  std::lock_guard<std::mutex> lk(g_pairs_mu);
+  int& n = g_max_pairs[dev][slot];
+  if (n <= 0) {
+    int smem = 0;
+    const void* fn = gemm_fn(mode, variant, &smem);
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    max_pairs[slot] = n > 0 ? n : 1;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    gemm_config(cfg, attr, smem, nullptr);
+    cfg.gridDim = dim3(num_sms);
+    int q = 0;
+    e = cudaOccupancyMaxActiveClusters(&q, fn, &cfg);
+    if (e != cudaSuccess) return e;
+    n = q > 0 ? q : 1;
   }
-  int pairs = max_pairs[slot] < num_sms / 2 ? max_pairs[slot] : num_sms / 2;
+  *pairs = n < num_sms / 2 ? n : num_sms / 2;
+  return cudaSuccess;
+}
+
+// Clusters of two CTAs (one pair per cluster), persistent: `pairs` pairs
+// (from ns_gemm_pairs), at most one per tile.
+cudaError_t launch_ns_gemm(int mode, int variant, const GemmParams& P, int pairs, cudaStream_t stream) {
+  int smem = 0;
+  const void* fn = gemm_fn(mode, variant, &smem);
   if (P.total_tiles < pairs) pairs = P.total_tiles;
   if (pairs <= 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[2];
+  gemm_config(cfg, attr, smem, stream);
   cfg.gridDim = dim3(2 * pairs);
   cfg.numAttrs = 2;
   void* args[] = {const_cast<GemmParams*>(&P)};

@@ -88,9 +88,44 @@ struct Fp8QuantParams {
   uint8_t* dst[2];
   long long n[2];
   float scale[2];
-  long long blocks0;  // blocks of tensor 0; the rest quantise tensor 1
+  float inv_scale[2];  // 1 / scale rounded to float (fast path of the quotient)
+  long long blocks0;   // blocks of tensor 0; the rest quantise tensor 1
 };
-constexpr int kQuantPerBlock = 256 * 8;
+constexpr int kQuantVecs = 4;  // 8-element vectors per thread, all in flight
+constexpr int kQuantPerBlock = 256 * 8 * kQuantVecs;
+
+// Operands of the FP8 product's backward (page section "自定义FP8矩阵乘法实现",
+// "反向传播优化"): per job, a rows x cols source in 128 x 128 tiles, written
+// transposed (cols x rows one-byte codes) and, for the gradient, also
+// row-major.  A gradient job quantises: code = E5M2(bf16(src / scale)); the
+// other jobs copy E4M3 codes.
+struct Fp8TJob {
+  const void* src;    // rows x cols: bf16 (quant) or one-byte codes
+  uint8_t* dst;       // rows x cols codes (quant jobs), else null
+  uint8_t* dst_t;     // cols x rows codes
+  int rows, cols;     // multiples of 16
+  int quant;          // 1: bf16 source quantised to E5M2
+  float scale, inv_scale;
+  int tiles_c;        // 128-column tiles across
+  int tile_begin;     // first block of this job
+  int pad;
+};
+constexpr int kFp8TJobs = 3;
+constexpr int kFp8Tile = 128;
+struct Fp8TParams {
+  Fp8TJob job[kFp8TJobs];
+  int n_jobs;
+};
+
+// Split-K reduction of an FP8 product: out = bf16(scale * sum over the
+// splits of part[split]) in a fixed order.
+struct Fp8ReduceParams {
+  const float* part;  // splits x n fp32
+  __nv_bfloat16* out; // n
+  long long n;        // a multiple of 4
+  int splits;
+  float scale;
+};
 
 // ---------------------------------------------------------------- GEMMs
 struct GemmClass {
@@ -110,18 +145,21 @@ struct GemmClass {
   int tile_begin;
   int mat_begin;
   int t4;                       // 1: tmT4 is valid (width a multiple of 64)
-  int pad[2];
+  int ksplit;                   // kFp8: the contraction is split in this
+                                //   many slices, each tile writing fp32
+                                //   partial sums through tmAux (1: none)
+  float scale;                  // kFp8: the product's scale
 };
 
 struct GemmParams {
   GemmClass cls[kMaxClasses];
   int n_classes;
   int total_tiles;
-  float ca, cb, cc;             // Newton-Schulz coefficients (kFp8: cc = x_s w_s)
+  float ca, cb, cc;             // Newton-Schulz coefficients
   int* status;
   long long wait_budget;        // clock64 cycles per barrier wait
   int inject_stall;             // test hook: MMA warp issues nothing
-  int pad;
+  uint32_t idesc_f8;            // kFp8: instruction descriptor (operand formats)
   long long* wait_profile;      // diagnostics: kWaitCounters per CTA, or null
   const MatInfo* table;         // update of the Muon step's last iteration:
   float lr;                     //   the matrices' parameters and the rate

@@ -291,10 +291,16 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
-// Instruction descriptor for kind::f8f6f4 with E4M3 A/B (format code 0),
-// both K-major, and an fp32 accumulator.
-__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+// Operand format codes of kind::f8f6f4.
+constexpr uint32_t kFmtE4M3 = 0;
+constexpr uint32_t kFmtE5M2 = 1;
+
+// Instruction descriptor for kind::f8f6f4 with 8-bit A and B of the given
+// formats (they may differ), both K-major, and an fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_f8(int M, int N, uint32_t a_fmt, uint32_t b_fmt) {
   return (1u << 4)                               // D format: f32
+         | (a_fmt << 7)                           // A format
+         | (b_fmt << 10)                          // B format
          | (static_cast<uint32_t>(N >> 3) << 17)  // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
 }

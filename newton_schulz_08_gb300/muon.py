@@ -33,14 +33,15 @@ MUON_F32 = 1
 EXPORTS = ["muon_workspace_size", "muon_step", "ns5_workspace_size", "ns5", "ns5_bank",
            "ns5_bank_workspace_size", "muon_device_status", "muon_status_str",
            "ns5_workspace_layout", "muon_set_debug", "muon_kernel_times", "ns5_noalloc",
-           "muon_partition", "adam_step", "fp8_mm"]
+           "muon_partition", "adam_step", "fp8_mm", "muon_plan_cache_clear",
+           "fp8_mm_backward", "fp8_mm_backward_workspace_size"]
 
 #: bytes of the static device scratch ns5_noalloc uses (MUON_NOALLOC_SCRATCH_BYTES)
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 #: kernel kinds reported by muon_kernel_times
 KERNEL_KINDS = ["momentum_cast", "normalise", "gram", "poly", "update", "apply", "update_apply", "fp8_quantize",
-                "fp8_mm"]
+                "fp8_mm", "fp8_transpose", "fp8_mm_bwd", "fp8_reduce"]
 
 
 class MuonError(RuntimeError):
@@ -112,6 +113,13 @@ def lib():
     L.adam_step.restype = c_int
     L.fp8_mm.argtypes = [c_vp, c_vp, c_f, c_f, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp, c_sz, c_vp]
     L.fp8_mm.restype = c_int
+    L.fp8_mm_backward_workspace_size.argtypes = [c_i64, c_i64, c_i64]
+    L.fp8_mm_backward_workspace_size.restype = c_sz
+    L.fp8_mm_backward.argtypes = [c_vp, c_vp, c_vp, c_f, c_f, c_f, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp,
+                                  c_sz, c_vp]
+    L.fp8_mm_backward.restype = c_int
+    L.muon_plan_cache_clear.argtypes = []
+    L.muon_plan_cache_clear.restype = None
     _lib = L
     return L
 
@@ -130,6 +138,21 @@ def _check(status, where, ok=(MUON_OK,)):
     if status not in ok:
         raise MuonError(status, where)
     return status
+
+
+def _device_of(tensors, what):
+    """The one CUDA device all `tensors` live on (raises otherwise).  The
+    library works on the current device with device pointers, so a CPU
+    tensor or a tensor of another GPU must never reach it."""
+    dev = None
+    for t in tensors:
+        if not t.is_cuda:
+            raise ValueError(f"{what}: every tensor must be a CUDA tensor")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"{what}: tensors are on {dev} and {t.device}; all must share one device")
+    return dev
 
 
 def _dtype_code(t):
@@ -175,10 +198,15 @@ def muon_step(params, grads, bufs, lr=0.02, momentum=0.95, nesterov=True, ns_ste
               workspace=None, stream=None):
     """One Muon step over a bank (lists of 2-D CUDA tensors), in place."""
     arr, n = _descs(params, grads, bufs)
-    if workspace is None:
-        workspace = new_workspace(lib().muon_workspace_size(arr, n), params[0].device)
-    st = lib().muon_step(arr, n, float(lr), float(momentum), int(bool(nesterov)), int(ns_steps),
-                         ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream(stream))
+    if n == 0:
+        return workspace
+    dev = _device_of(list(params) + list(grads) + list(bufs) + ([workspace] if workspace is not None else []),
+                     "muon_step")
+    with torch.cuda.device(dev):
+        if workspace is None:
+            workspace = new_workspace(lib().muon_workspace_size(arr, n), dev)
+        st = lib().muon_step(arr, n, float(lr), float(momentum), int(bool(nesterov)), int(ns_steps),
+                             ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream(stream))
     _check(st, "muon_step")
     return workspace
 
@@ -198,11 +226,13 @@ def ns5(G, ns_steps=5, out=None, workspace=None, stream=None):
         out = torch.empty(G3.shape, dtype=torch.bfloat16, device=G.device)
     if out.shape != G3.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
         raise ValueError("out must be a contiguous bfloat16 tensor shaped like G")
-    if workspace is None:
-        workspace = new_workspace(ns5_workspace_size(batch, rows, cols) if batch else 256, G.device)
-    st = lib().ns5(ctypes.c_void_p(G3.data_ptr()), _dtype_code(G3), ctypes.c_void_p(out.data_ptr()),
-                   batch, rows, cols, int(ns_steps), ctypes.c_void_p(workspace.data_ptr()),
-                   workspace.numel(), _stream(stream))
+    dev = _device_of([G3, out] + ([workspace] if workspace is not None else []), "ns5")
+    with torch.cuda.device(dev):
+        if workspace is None:
+            workspace = new_workspace(ns5_workspace_size(batch, rows, cols) if batch else 256, dev)
+        st = lib().ns5(ctypes.c_void_p(G3.data_ptr()), _dtype_code(G3), ctypes.c_void_p(out.data_ptr()),
+                       batch, rows, cols, int(ns_steps), ctypes.c_void_p(workspace.data_ptr()),
+                       workspace.numel(), _stream(stream))
     _check(st, "ns5")
     return out[0] if squeeze else out
 
@@ -225,16 +255,19 @@ def ns5_bank(Gs, ns_steps=5, outs=None, workspace=None, stream=None):
         if (g.dim() != 2 or not g.is_contiguous() or o.shape != g.shape or o.dtype != torch.bfloat16
                 or not o.is_contiguous()):
             raise ValueError("each G must be 2-D contiguous with a contiguous bf16 out of the same shape")
+    if n == 0:
+        return outs
+    dev = _device_of(list(Gs) + list(outs) + ([workspace] if workspace is not None else []), "ns5_bank")
     gp = (ctypes.c_void_p * max(n, 1))(*[g.data_ptr() for g in Gs])
     op = (ctypes.c_void_p * max(n, 1))(*[o.data_ptr() for o in outs])
     dt = (ctypes.c_int32 * max(n, 1))(*[_dtype_code(g) for g in Gs])
     rows = (ctypes.c_int64 * max(n, 1))(*[g.shape[0] for g in Gs])
     cols = (ctypes.c_int64 * max(n, 1))(*[g.shape[1] for g in Gs])
-    if workspace is None:
-        workspace = new_workspace(lib().ns5_bank_workspace_size(rows, cols, n) if n else 256,
-                                  Gs[0].device if n else None)
-    st = lib().ns5_bank(gp, dt, op, rows, cols, n, int(ns_steps),
-                        ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream(stream))
+    with torch.cuda.device(dev):
+        if workspace is None:
+            workspace = new_workspace(lib().ns5_bank_workspace_size(rows, cols, n), dev)
+        st = lib().ns5_bank(gp, dt, op, rows, cols, n, int(ns_steps),
+                            ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _stream(stream))
     _check(st, "ns5_bank")
     return outs
 
@@ -250,6 +283,11 @@ def ns5_workspace_layout(batch, rows, cols):
            "ns5_workspace_layout")
     return {"x_offset": (out.x_offset[0], out.x_offset[1]), "a_offset": out.a_offset,
             "b_offset": out.b_offset, "ldx": out.ldx, "lda": out.lda, "m": out.m, "n": out.n}
+
+
+def muon_plan_cache_clear():
+    """Drop the library's prepared calls (host memory only)."""
+    lib().muon_plan_cache_clear()
 
 
 def muon_set_debug(key, value):
@@ -280,9 +318,13 @@ def ns5_noalloc(G, ns_steps=5, out=None, stream=None):
         out = torch.empty(G3.shape, dtype=torch.bfloat16, device=G.device)
     if out.shape != G3.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
         raise ValueError("out must be a contiguous bfloat16 tensor shaped like G")
-    st = lib().ns5_noalloc(ctypes.c_void_p(G3.data_ptr()), _dtype_code(G3),
-                           ctypes.c_void_p(out.data_ptr()), batch, rows, cols, int(ns_steps),
-                           _stream(stream))
+    dev = _device_of([G3, out], "ns5_noalloc")
+    # the library's scratch array and the default stream are the current
+    # device's: make G's device current for the call
+    with torch.cuda.device(dev):
+        st = lib().ns5_noalloc(ctypes.c_void_p(G3.data_ptr()), _dtype_code(G3),
+                               ctypes.c_void_p(out.data_ptr()), batch, rows, cols, int(ns_steps),
+                               _stream(stream))
     _check(st, "ns5_noalloc")
     return out[0] if squeeze else out
 
@@ -316,8 +358,12 @@ def adam_step(params, grads, exp_avgs, exp_avg_sqs, step, lr=1e-3, beta1=0.9, be
             raise ValueError("tensor sizes differ or a gradient is not contiguous")
         arr[i] = adam_tensor_desc(p.data_ptr(), g.data_ptr(), m.data_ptr(), v.data_ptr(), p.numel(),
                                   _dtype_code(g), 0)
-    st = lib().adam_step(arr, n, float(lr), float(beta1), float(beta2), float(eps), float(weight_decay),
-                         int(step), int(bool(cautious)), _stream(stream))
+    if n == 0:
+        return
+    dev = _device_of(list(params) + list(grads) + list(exp_avgs) + list(exp_avg_sqs), "adam_step")
+    with torch.cuda.device(dev):
+        st = lib().adam_step(arr, n, float(lr), float(beta1), float(beta2), float(eps), float(weight_decay),
+                             int(step), int(bool(cautious)), _stream(stream))
     _check(st, "adam_step")
 
 
@@ -348,11 +394,57 @@ def fp8_mm(x, w, x_s, w_s, out=None, x_f8=None, w_f8=None, workspace=None, strea
     x_f8, w_f8 = x_f8.view(torch.uint8), w_f8.view(torch.uint8)
     if w.device != dev:
         raise ValueError("x and w must be on the same device")
-    if workspace is None:
-        workspace = new_workspace(256, dev)
-    st = lib().fp8_mm(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(w.data_ptr()), float(x_s), float(w_s),
-                      ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(x_f8.data_ptr()),
-                      ctypes.c_void_p(w_f8.data_ptr()), M, N, K, ctypes.c_void_p(workspace.data_ptr()),
-                      workspace.numel(), _stream(stream))
+    _device_of([x, w, out, x_f8, w_f8] + ([workspace] if workspace is not None else []), "fp8_mm")
+    with torch.cuda.device(dev):
+        if workspace is None:
+            workspace = new_workspace(256, dev)
+        st = lib().fp8_mm(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(w.data_ptr()), float(x_s), float(w_s),
+                          ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(x_f8.data_ptr()),
+                          ctypes.c_void_p(w_f8.data_ptr()), M, N, K, ctypes.c_void_p(workspace.data_ptr()),
+                          workspace.numel(), _stream(stream))
     _check(st, "fp8_mm")
     return out, x_f8.view(torch.float8_e4m3fn), w_f8.view(torch.float8_e4m3fn)
+
+
+def fp8_mm_backward_workspace_size(M, N, K):
+    return lib().fp8_mm_backward_workspace_size(int(M), int(N), int(K))
+
+
+def fp8_mm_backward(g, x_f8, w_f8, x_s, w_s, grad_s, grad_x=None, grad_w=None, g_f8=None, workspace=None,
+                    stream=None):
+    """Backward of the FP8 scaled product: g (M x N bf16) and the forward's
+    x_f8 (M x K) and w_f8 (N x K) E4M3 codes -> (grad_x, grad_w, g_f8):
+    grad_x = bf16(grad_s w_s (g_f8 . w_f8)), grad_w = bf16(grad_s x_s
+    (g_f8^T . x_f8)), g_f8 = E5M2(bf16(g / grad_s)) as a float8_e5m2 tensor.
+    See fp8_mm_backward in include/muon.h."""
+    if g.dim() != 2 or g.dtype != torch.bfloat16 or not g.is_contiguous():
+        raise ValueError("g must be a contiguous 2-D bfloat16 CUDA tensor")
+    M, N = g.shape
+    for t, shape in ((x_f8, None), (w_f8, None)):
+        if t.dim() != 2 or t.element_size() != 1 or not t.is_contiguous():
+            raise ValueError("x_f8 / w_f8 must be contiguous 2-D one-byte tensors")
+    K = x_f8.shape[1]
+    if x_f8.shape != (M, K) or w_f8.shape != (N, K):
+        raise ValueError("x_f8 must be M x K and w_f8 N x K for g of M x N")
+    dev = _device_of([g, x_f8, w_f8] + [t for t in (grad_x, grad_w, g_f8, workspace) if t is not None],
+                     "fp8_mm_backward")
+    grad_x = torch.empty((M, K), dtype=torch.bfloat16, device=dev) if grad_x is None else grad_x
+    grad_w = torch.empty((N, K), dtype=torch.bfloat16, device=dev) if grad_w is None else grad_w
+    g_f8 = torch.empty((M, N), dtype=torch.uint8, device=dev) if g_f8 is None else g_f8
+    for t, shape in ((grad_x, (M, K)), (grad_w, (N, K))):
+        if t.shape != shape or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("grad_x / grad_w must be contiguous bfloat16 tensors of M x K / N x K")
+    if (g_f8.shape != (M, N) or g_f8.element_size() != 1 or not g_f8.is_contiguous()
+            or g_f8.dtype not in (torch.uint8, torch.float8_e5m2)):
+        raise ValueError("g_f8 must be a contiguous M x N one-byte tensor (uint8 or float8_e5m2)")
+    g_f8 = g_f8.view(torch.uint8)
+    with torch.cuda.device(dev):
+        if workspace is None:
+            workspace = new_workspace(fp8_mm_backward_workspace_size(M, N, K), dev)
+        st = lib().fp8_mm_backward(ctypes.c_void_p(g.data_ptr()), ctypes.c_void_p(x_f8.data_ptr()),
+                                   ctypes.c_void_p(w_f8.data_ptr()), float(x_s), float(w_s), float(grad_s),
+                                   ctypes.c_void_p(grad_x.data_ptr()), ctypes.c_void_p(grad_w.data_ptr()),
+                                   ctypes.c_void_p(g_f8.data_ptr()), M, N, K, ctypes.c_void_p(workspace.data_ptr()),
+                                   workspace.numel(), _stream(stream))
+    _check(st, "fp8_mm_backward")
+    return grad_x, grad_w, g_f8.view(torch.float8_e5m2)

@@ -39,6 +39,12 @@ def test_exports_every_declared_symbol(L):
         assert hasattr(L, n), n
 
 
+def test_plan_cache_clear_is_host_only(L):
+    # drops host memory only: callable with no GPU and no prepared call
+    muon.muon_plan_cache_clear()
+    muon.muon_plan_cache_clear()
+
+
 def test_status_strings(L):
     for code in range(-8, 2):
         assert muon.muon_status_str(code)
@@ -234,3 +240,60 @@ def test_ns5_bank_binding_checks_outs():
         muon.ns5_bank(G, 5, outs=[torch.zeros((4, 8), dtype=torch.bfloat16), torch.zeros((4, 8), dtype=torch.bfloat16)])
     with pytest.raises(ValueError):
         muon.ns5_bank([torch.zeros(8)], 5)  # not 2-D
+
+
+def test_fp8_backward_workspace_size(L):
+    assert muon.fp8_mm_backward_workspace_size(0, 16, 16) == 256
+    assert muon.fp8_mm_backward_workspace_size(17, 16, 16) == 0
+    assert muon.fp8_mm_backward_workspace_size(-16, 16, 16) == 0
+    # status word, then the transposed copies of g_f8 (N x M), x_f8 (K x M)
+    # and w_f8 (K x N), 1 KiB aligned; 36 output tiles of grad_w split twice
+    M, N, K = 65536, 3072, 768
+    size = muon.fp8_mm_backward_workspace_size(M, N, K)
+    copies = 1024 + N * M + K * M + K * N
+    assert size == copies + 2 * N * K * 4
+    # enough output tiles: no partial sums
+    assert muon.fp8_mm_backward_workspace_size(256, 4096, 4096) == 1024 + 4096 * 256 * 2 + 4096 * 4096
+
+
+@pytest.mark.parametrize("case,code", [
+    ("ragged_m", muon.MUON_ERR_INVALID_ARG),
+    ("neg_k", muon.MUON_ERR_INVALID_ARG),
+    ("null_g", muon.MUON_ERR_INVALID_ARG),
+    ("zero_scale", muon.MUON_ERR_INVALID_ARG),
+    ("nan_scale", muon.MUON_ERR_INVALID_ARG),
+    ("misaligned_out", muon.MUON_ERR_MISALIGNED),
+    ("misaligned_ws", muon.MUON_ERR_MISALIGNED),
+    ("ws_small", muon.MUON_ERR_WORKSPACE_TOO_SMALL),
+    ("alias_out_in", muon.MUON_ERR_ALIASING),
+    ("alias_ws", muon.MUON_ERR_ALIASING),
+])
+def test_fp8_backward_argument_errors(L, case, code):
+    M, N, K = 64, 32, 48
+    a = dict(g=0x1000000, x=0x2000000, w=0x3000000, gx=0x4000000, gw=0x5000000, gq=0x6000000,
+             xs=1.0, ws_=1.0, gs=1.0, M=M, N=N, K=K, wsp=0x8000000,
+             wsb=muon.fp8_mm_backward_workspace_size(M, N, K))
+    if case == "ragged_m":
+        a["M"] = 60
+    elif case == "neg_k":
+        a["K"] = -16
+    elif case == "null_g":
+        a["g"] = 0
+    elif case == "zero_scale":
+        a["gs"] = 0.0
+    elif case == "nan_scale":
+        a["xs"] = float("nan")
+    elif case == "misaligned_out":
+        a["gx"] += 8
+    elif case == "misaligned_ws":
+        a["wsp"] += 16
+    elif case == "ws_small":
+        a["wsb"] -= 1
+    elif case == "alias_out_in":
+        a["gx"] = a["g"] + 64
+    elif case == "alias_ws":
+        a["gw"] = a["wsp"] + 256
+    vp = ctypes.c_void_p
+    st = L.fp8_mm_backward(vp(a["g"]), vp(a["x"]), vp(a["w"]), a["xs"], a["ws_"], a["gs"], vp(a["gx"]), vp(a["gw"]),
+                           vp(a["gq"]), a["M"], a["N"], a["K"], vp(a["wsp"]), a["wsb"], None)
+    assert st == code

@@ -4,9 +4,11 @@ the GPU, or latency-critical code where cudaMalloc could synchronise the
 device).  It runs the same kernels as ns5 but takes its scratch from a static
 64 MiB device array inside the library instead of a caller workspace.
 
-The GPU test calls it through the C ABI twice in a row, on different shapes
-and dtypes, and compares each result with ns5 given a normal workspace.  The
-file is named so that pytest collects it last.
+The GPU tests call it through the C ABI twice in a row, on different shapes
+and dtypes, and compare each result with ns5 given a normal workspace; and
+check that, once the first call has loaded the library's device code, calls
+change neither the memory PyTorch's allocator holds nor the device's free
+memory.  The file is named so that pytest collects it last.
 """
 
 import ctypes
@@ -56,3 +58,18 @@ def test_noalloc_matches_ns5_on_two_calls_in_a_row():
         assert np.abs(got - want).max() <= TOL_MAXABS_BF16
         # same kernels, same arithmetic: the results are in fact identical
         assert torch.equal(out, ref)
+
+
+@pytest.mark.gpu
+def test_noalloc_calls_allocate_no_device_memory():
+    rng = np.random.default_rng(7)
+    G = torch.from_numpy(rng.standard_normal((2, 384, 640)).astype(np.float32)).cuda()
+    out = torch.empty(G.shape, dtype=torch.bfloat16, device="cuda")
+    assert call_noalloc(G, out) == muon.MUON_OK  # loads the module, reserves the array
+    torch.cuda.synchronize()
+    held, (free, _) = torch.cuda.memory_allocated(), torch.cuda.mem_get_info()
+    for _ in range(2):
+        assert call_noalloc(G, out) == muon.MUON_OK
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated() == held
+    assert torch.cuda.mem_get_info()[0] == free
