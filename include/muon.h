@@ -140,10 +140,10 @@ const char* muon_status_str(muon_status_t status);
 /* Where ns5 keeps its bfloat16 buffers inside the workspace (for tests and
  * inspection): byte offsets of the two X buffers, of A and of B, the row
  * pitches in elements, and m = min(rows, cols), n = max(rows, cols).  After
- * ns5 with ns_steps = k >= 1: A holds step k's A (for m <= 768 only its
- * 256 x 256 blocks on and above the diagonal: A is symmetric and blocks below
- * the diagonal are not written; wider A whole), B holds step k's B whole, and
- * X buffer (k % 2) holds step k's X (m x n, transposed for tall input); with
+ * ns5 with ns_steps = k >= 1: A and B hold step k's A and B (for m <= 768
+ * only their 256 x 256 blocks on and above the diagonal: both are symmetric
+ * and blocks below the diagonal are not written; wider ones whole), and X
+ * buffer (k % 2) holds step k's X (m x n, transposed for tall input); with
  * k = 0, X buffer 0 holds X0. */
 typedef struct muon_ws_layout {
   size_t x_offset[2];

@@ -427,17 +427,17 @@ muon_status_t prepare(const std::vector<JobMat>& mats, const Plan& P, int ns_ste
     const int src = t & 1, dst = src ^ 1;
     for (size_t c0 = 0; c0 < P.cls.size(); c0 += kMaxClasses) {
       const int nc = static_cast<int>(std::min<size_t>(kMaxClasses, P.cls.size() - c0));
-      // Gram and polynomial: classes whose A is stored block-upper (m up to
-      // kSymUpperMaxM) and the others go to separate kernel instantiations
+      // classes whose A and B are stored block-upper (m up to kSymUpperMaxM)
+      // and the others go to separate kernel instantiations
       for (int mode = kGram; mode <= kUpdate; ++mode) {
-        for (int sym = 0; sym <= (mode == kUpdate ? 0 : 1); ++sym) {
+        for (int sym = 0; sym <= 1; ++sym) {
           GemmParams gp;
           std::memset(&gp, 0, sizeof(gp));
           int tiles = 0;
           int ng = 0;
           for (int j = 0; j < nc; ++j) {
             const ClassPlan& cp = P.cls[c0 + j];
-            if (mode != kUpdate && (cp.m <= kSymUpperMaxM ? 1 : 0) != sym) continue;
+            if ((cp.m <= kSymUpperMaxM ? 1 : 0) != sym) continue;
             GemmClass& g = gp.cls[ng++];
             void* xs = ws + cp.x_off[src];
             void* xd = ws + cp.x_off[dst];
@@ -470,8 +470,10 @@ muon_status_t prepare(const std::vector<JobMat>& mats, const Plan& P, int ns_ste
               g.K = cp.m;
             }
             if (!ok) return MUON_ERR_CUDA;
-            // poly: one-copy transposed reads of A where the width allows
-            g.t4 = mode == kPoly && sym && encode_map4(&g.tmT4, A, cp.m, cp.m, cp.count, cp.lda);
+            // poly / update: one-copy transposed reads of A / B where the
+            // width allows
+            g.t4 = (mode == kPoly || mode == kUpdate) && sym &&
+                   encode_map4(&g.tmT4, mode == kPoly ? A : B, cp.m, cp.m, cp.count, cp.lda);
             // mirrored entries of the Gram (wide A) and the polynomial (B)
             if (mode != kUpdate && !encode_map(&g.tmMir, mode == kGram ? A : B, cp.m, cp.m, cp.count, cp.lda, 32,
                                                64, CU_TENSOR_MAP_SWIZZLE_NONE))
@@ -501,7 +503,7 @@ muon_status_t prepare(const std::vector<JobMat>& mats, const Plan& P, int ns_ste
           // the Muon step's last update applies p -= lr X' itself
           gp.table = table;
           gp.apply = mode == kUpdate && final_mode == kFinalParam && t == ns_steps - 1;
-          const int variant = mode == kUpdate ? gp.apply : sym;
+          const int variant = sym | (gp.apply << 1);
           int pairs = 0;
           if (ns_gemm_pairs(mode, variant, sms, &pairs) != cudaSuccess) return MUON_ERR_CUDA;
           Q.seq.push_back({kLGemm, gp.apply ? 6 : 2 + mode, pairs, mode, variant, static_cast<int>(Q.gemm.size())});

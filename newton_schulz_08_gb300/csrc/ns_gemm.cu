@@ -17,11 +17,13 @@
 //             block-upper structure applies with K = m.  Where A is stored
 //             block-upper, operand blocks below the diagonal are loaded from
 //             the stored block above it as MN-major operands (one 4-D copy
-//             per 128 x 64 half where the width is a multiple of 64).  The
-//             epilogue reads A's (upper) tile, fuses b A + c (.), and also
-//             writes the mirrored entries, so B is stored whole.
+//             per 128 x 64 half where the width is a multiple of 64), and B
+//             is stored block-upper as well; for wider matrices the epilogue
+//             also writes the mirrored entries, so B is stored whole.  The
+//             epilogue reads A's (upper) tile and fuses b A + c (.).
 //   kUpdate : X' = a X + B X.     All tiles of the m x n result; B is the
-//             K-major A operand, X the MN-major B operand.  The epilogue
+//             A operand (K-major, or MN-major where a block-upper B is read
+//             below its diagonal), X the MN-major B operand.  The epilogue
 //             reads X's tile and fuses a X + (.).  In the last step of the
 //             Muon step it applies p <- p - lr X' (fp32, in p's own layout)
 //             instead of storing X'.
@@ -137,11 +139,11 @@ __device__ __forceinline__ float word_hi(uint32_t w) { return __uint_as_float(w 
 
 }  // namespace
 
-// SYM (Gram and polynomial only): 1 for classes whose A is stored as its
-// blocks on and above the diagonal only (m <= kSymUpperMaxM): the Gram writes
-// no mirrored entries and the polynomial reads the blocks below the diagonal
-// transposed.  A compile-time choice, so that the other classes run code
-// without any of it.
+// SYM: 1 for classes whose A and B are stored as their blocks on and above
+// the diagonal only (m <= kSymUpperMaxM): the Gram and the polynomial write
+// no mirrored entries, the polynomial reads A's blocks below the diagonal
+// transposed and the update reads B's.  A compile-time choice, so that the
+// other classes run code without any of it.
 // APPLY (update only): the Muon step's last update, which applies
 // p <- p - lr X' instead of storing X'; also compile-time, so that the other
 // updates run without its registers.
@@ -255,7 +257,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
                 ptx::tma_load_3d_pair(dst + j * (64 * kBK * 2), &C.tmT, fb, col + 64 * j, kb * kBK, tl.idx);
             }
           };
-          if (MODE == kPoly && SYM && jb < tl.I) {
+          if ((MODE == kPoly || MODE == kUpdate) && SYM && jb < tl.I) {
             load_t(sa, tl.I * kBM + half);
           } else {
             ptx::tma_load_3d_pair(sa, &C.tmA, fb, kb * kKB, tl.I * kBM + half, tl.idx);
@@ -318,7 +320,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           const uint32_t sa = ptx::smem_addr(smem + stage * kStageBytes);
           const uint32_t sb = sa + kStageA;
           const int jb = kb * kBK / kBN;
-          const bool a_mn = MODE == kPoly && SYM && jb < tl.I;
+          const bool a_mn = (MODE == kPoly || MODE == kUpdate) && SYM && jb < tl.I;
           const bool b_mn = MODE == kUpdate || (MODE == kPoly && SYM && jb < tl.J);
           const uint32_t idesc = a_mn ? (b_mn ? idesc_mm : idesc_mk) : (b_mn ? idesc_km : idesc_kk);
 #pragma unroll
@@ -590,8 +592,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           }
         }
       }
-      if ((MODE == kPoly || (MODE == kGram && !SYM)) && tl.I != tl.J) {
-        // B (and A of wide matrices) is stored whole: the mirrored entries
+      if ((MODE == kPoly || MODE == kGram) && !SYM && tl.I != tl.J) {
+        // A and B of wide matrices are stored whole: the mirrored entries
         // (r, c) -> (c, r) of the warp's 32 rows go through its first staging
         // slot transposed, 64 columns at a time: row c of the slot holds the
         // 32 values of column c (64 bytes, unswizzled, one store instruction
@@ -665,28 +667,34 @@ template __global__ void ns_gemm_kernel<kPoly, 0, 0>(const __grid_constant__ Gem
 template __global__ void ns_gemm_kernel<kPoly, 1, 0>(const __grid_constant__ GemmParams P);
 template __global__ void ns_gemm_kernel<kUpdate, 0, 0>(const __grid_constant__ GemmParams P);
 template __global__ void ns_gemm_kernel<kUpdate, 0, 1>(const __grid_constant__ GemmParams P);
+template __global__ void ns_gemm_kernel<kUpdate, 1, 0>(const __grid_constant__ GemmParams P);
+template __global__ void ns_gemm_kernel<kUpdate, 1, 1>(const __grid_constant__ GemmParams P);
 template __global__ void ns_gemm_kernel<kFp8, 0, 0>(const __grid_constant__ GemmParams P);
 
 // ------------------------------------------------------------------ launcher
 namespace {
 
 // The kernel instantiation of a (mode, variant) and its shared memory.
-// Variant: Gram / polynomial 1 = A stored block-upper; update 1 = with the
-// parameter update; FP8 0.
+// Variant bit 0: A (and B) stored block-upper (Gram, polynomial, update);
+// bit 1: the update with the parameter update.  FP8: 0.
 const void* gemm_fn(int mode, int variant, int* smem) {
   switch (mode) {
     case kGram:
       *smem = GemmShape<kGram>::smem;
-      return variant ? reinterpret_cast<const void*>(&ns_gemm_kernel<kGram, 1, 0>)
-                     : reinterpret_cast<const void*>(&ns_gemm_kernel<kGram, 0, 0>);
+      return variant & 1 ? reinterpret_cast<const void*>(&ns_gemm_kernel<kGram, 1, 0>)
+                         : reinterpret_cast<const void*>(&ns_gemm_kernel<kGram, 0, 0>);
     case kPoly:
       *smem = GemmShape<kPoly>::smem;
-      return variant ? reinterpret_cast<const void*>(&ns_gemm_kernel<kPoly, 1, 0>)
-                     : reinterpret_cast<const void*>(&ns_gemm_kernel<kPoly, 0, 0>);
+      return variant & 1 ? reinterpret_cast<const void*>(&ns_gemm_kernel<kPoly, 1, 0>)
+                         : reinterpret_cast<const void*>(&ns_gemm_kernel<kPoly, 0, 0>);
     case kUpdate:
       *smem = GemmShape<kUpdate>::smem;
-      return variant ? reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate, 0, 1>)
-                     : reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate, 0, 0>);
+      switch (variant & 3) {
+        case 0: return reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate, 0, 0>);
+        case 1: return reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate, 1, 0>);
+        case 2: return reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate, 0, 1>);
+        default: return reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate, 1, 1>);
+      }
     default:
       *smem = GemmShape<kFp8>::smem;
       return reinterpret_cast<const void*>(&ns_gemm_kernel<kFp8, 0, 0>);
@@ -709,7 +717,7 @@ void gemm_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[2], int sm
 }
 
 constexpr int kMaxGemmDevices = 64;
-constexpr int kGemmSlots = 8;  // mode * 2 + variant
+constexpr int kGemmSlots = 16;  // mode * 4 + variant
 std::mutex g_pairs_mu;
 int g_max_pairs[kMaxGemmDevices][kGemmSlots] = {};
 
@@ -724,7 +732,7 @@ cudaError_t ns_gemm_pairs(int mode, int variant, int num_sms, int* pairs) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxGemmDevices) return cudaErrorInvalidDevice;
-  const int slot = mode * 2 + variant;
+  const int slot = mode * 4 + variant;
   std::lock_guard<std::mutex> lk(g_pairs_mu);
   int& n = g_max_pairs[dev][slot];
   if (n <= 0) {

@@ -67,13 +67,11 @@ def test_one_step_each_kernel(shape):
     X0 = ws_view(ws, lay["x_offset"][0], m, n, ldx)
     A_st = ws_view(ws, lay["a_offset"], m, m, lda)
     B_st = ws_view(ws, lay["b_offset"], m, m, lda)
-    # A is stored as its 256 x 256 blocks on and above the diagonal (diagonal
-    # blocks computed whole, exactly symmetric); B is stored whole and is
-    # exactly symmetric
-    assert diagonal_blocks_symmetric(A_st)
+    # A and B are stored as their 256 x 256 blocks on and above the diagonal
+    # (diagonal blocks computed whole, exactly symmetric)
+    assert diagonal_blocks_symmetric(A_st) and diagonal_blocks_symmetric(B_st)
     A = sym_from_upper_blocks(A_st)
-    assert np.array_equal(B_st, B_st.T)
-    B = B_st
+    B = sym_from_upper_blocks(B_st)
     X1 = ws_view(ws, lay["x_offset"][1], m, n, ldx)
     # X0 is the oracle's normalised input (orientation: tall inputs transposed)
     Gv, tall = oracle.orient(G.astype(np.float64))
