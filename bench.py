@@ -20,11 +20,14 @@ steps, parameter update (18 kernel launches through the C ABI).
              on a bounded sample of the bank's matrices
 
 ``--impl reference`` times the CPU oracle as the reference arm (rank 0 only).
-Multi-GPU (torchrun, N ranks): every matrix's step depends on that matrix
-alone, so the units shard with no exchange of data.  The bank is repeated N
-times (weak scaling: one bank's work per GPU) and split between the ranks by
-the library's work-balanced partition (muon_partition); each rank updates the
-matrices it owns.  value = matrices of all ranks / max time over ranks.
+Multi-GPU (torchrun, N ranks): the data-parallel step of sharded.ShardedBank.
+The bank is repeated N times (weak scaling: one bank's Newton-Schulz work per
+GPU) and every rank holds all of it; matrices are owned by the library's
+work-balanced partition (muon_partition).  Per size group: a reduce-scatter
+of the bf16 gradients, the owners' muon_step, an asynchronous all-gather of
+the parameters.  value = matrices of the whole bank / max time over ranks.
+``--sharded`` runs the same path on one rank.  The Adam and FP8 workloads run
+one independent copy per rank.
 """
 
 import argparse
@@ -479,6 +482,74 @@ def views(flat, shapes):
     return out
 
 
+def secondary_spectra(device, steps=5, warmup=3):
+    """A short spectra sweep (ns5_bank over 64 x 1024^2 + 16 x 4096^2 bf16,
+    5 Newton-Schulz steps) timed in the same process as the headline line:
+    ms per sweep, per-kernel fractions of the measured peaks and the clocks
+    seen meanwhile.  It puts the 4096-wide kernels' rate into the record."""
+    import ctypes
+
+    import torch
+
+    from newton_schulz_08_gb300 import inputs, muon
+    L = muon.lib()
+    shapes = inputs.spectra_shapes()
+    n = len(shapes)
+    total = sum(r * c for r, c in shapes)
+    G = torch.empty(total, dtype=torch.bfloat16, device=device)
+    off = 0
+    for i, (r, c) in enumerate(shapes):
+        G[off:off + r * c].copy_(inputs.spectra_matrix_device(r, i, device, torch.bfloat16).reshape(-1))
+        off += r * c
+    O = torch.empty_like(G)
+    gp = (ctypes.c_void_p * n)(*[g.data_ptr() for g in views(G, shapes)])
+    op = (ctypes.c_void_p * n)(*[o.data_ptr() for o in views(O, shapes)])
+    dt = (ctypes.c_int32 * n)(*([muon.MUON_BF16] * n))
+    rows = (ctypes.c_int64 * n)(*[r for r, _ in shapes])
+    cols = (ctypes.c_int64 * n)(*[c for _, c in shapes])
+    ws = muon.new_workspace(L.ns5_bank_workspace_size(rows, cols, n), device)
+    stream = torch.cuda.current_stream(device)
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+
+    def sweep():
+        st = L.ns5_bank(gp, dt, op, rows, cols, n, NS_STEPS, ctypes.c_void_p(ws.data_ptr()), ws.numel(), sptr)
+        if st != 0:
+            raise muon.MuonError(st, "ns5_bank")
+
+    for _ in range(max(warmup, 3)):
+        sweep()
+    torch.cuda.synchronize(device)
+    clocks = ClockSampler(device.index or 0)
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        sweep()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / steps
+    muon.muon_set_debug("record_kernel_events", 1)
+    muon.muon_kernel_times()
+    for _ in range(steps):
+        sweep()
+    torch.cuda.synchronize(device)
+    kt = muon.muon_kernel_times()
+    muon.muon_set_debug("record_kernel_events", 0)
+    clk = clocks.stop()
+    if muon.muon_device_status(ws) != 0:
+        raise RuntimeError("device status after the spectra sweep")
+    peaks, src = load_peaks()
+    kern = kernel_report(kt, steps, ns_flops(shapes), ns_flops_issued(shapes), hbm_bytes(shapes, 2, True), peaks)
+    flops = sum(ns_flops(shapes).values())
+    return {
+        "workload": WORKLOAD_DESC["spectra"], "steps": steps, "ms_per_sweep": ms,
+        "matrices_per_s": n / (ms * 1e-3), "ns5_tflops": flops / (ms * 1e-3) / 1e12,
+        "kernels": {k: {"avg_ms": v["avg_ms"], "frac": v["frac"], "issued_frac": v.get("issued_frac"),
+                        "unit": v["unit"], "achieved": v["achieved"]} for k, v in kern.items()},
+        "peak_source": src, "clocks": clk,
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -488,6 +559,9 @@ def main():
     ap.add_argument("--workload", default="gpt2", choices=sorted(WORKLOAD_DESC))
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of CPU oracle work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true", help="skip the spectra sweep of the gpt2 line")
+    ap.add_argument("--sharded", action="store_true",
+                    help="time the sharded data-parallel step (the default when more than one rank runs)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -515,6 +589,9 @@ def main():
         return
     if args.workload == "fp8":
         run_fp8(args, rank, world, device)
+        return
+    if (world > 1 or args.sharded) and args.workload not in NS5_ONLY:
+        run_sharded(args, rank, world, device)
         return
 
     L = muon.lib()
@@ -679,15 +756,139 @@ def main():
         "gpu_launches_note": "kernels launched in the per-kernel timing pass (same count as the main timed loop)",
         "clocks": clk,
     }
+    if world == 1 and args.workload == "gpt2" and not args.no_secondary:
+        line["secondary"] = secondary_spectra(device)
     if world == 1 and not args.no_cpu_baseline and not ns5_only:
         n_cpu, t_cpu = oracle_sample(shapes, args.cpu_budget)
-        line["cpu_baseline"] = {"value": n_cpu / t_cpu, "unit": "matrices/s", "cores": cpu_threads(),
-                                "kind": "oracle",
-                                "sample": f"{n_cpu} matrices of the bank in order, full Muon step, "
-                                          f"bf16-emulating oracle, {t_cpu:.1f} s"}
+        n64, t64 = oracle_sample(shapes, args.cpu_budget / 2, mode="fp64")
+        per_bank = len(shapes)
+        line["cpu_baseline"] = {
+            "value": n_cpu / t_cpu, "unit": "matrices/s", "cores": cpu_threads(), "kind": "oracle",
+            "sample": f"{n_cpu} matrices of the bank in order, full Muon step, bf16-emulating oracle, "
+                      f"{t_cpu:.1f} s (capped; a full {per_bank}-matrix step extrapolates to "
+                      f"{per_bank * t_cpu / n_cpu:.1f} s)",
+            "fp64": {"value": n64 / t64, "unit": "matrices/s",
+                     "sample": f"{n64} matrices in order, fp64 oracle, {t64:.1f} s (capped; a full step "
+                               f"extrapolates to {per_bank * t64 / n64:.1f} s)"}}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def run_sharded(args, rank, world, device):
+    """The data-parallel Muon step (sharded.ShardedBank) over `world` ranks:
+    the bank repeated `world` times (weak scaling: one bank's Newton-Schulz
+    work per GPU, while the exchange covers the whole world-sized bank),
+    every rank holding all parameters and its own gradients for all of them;
+    per size group one reduce-scatter of the bf16 gradients, the owners'
+    muon_step, one asynchronous all-gather of the parameters."""
+    import torch
+    import torch.distributed as dist
+
+    from newton_schulz_08_gb300 import inputs, muon, sharded
+
+    if not dist.is_initialized():
+        # one rank (--sharded): a process group of its own, so that the same
+        # collectives run (as copies)
+        import socket
+        with socket.socket() as sk:
+            sk.bind(("127.0.0.1", 0))
+            port = sk.getsockname()[1]
+        store = dist.TCPStore("127.0.0.1", port, 1, True)
+        dist.init_process_group("nccl", store=store, rank=0, world_size=1, device_id=device)
+    base = workload_shapes(args.workload)
+    shapes = [base[g % len(base)] for g in range(len(base) * world)]
+    bank = sharded.ShardedBank(shapes, device)
+    for i, s in enumerate(shapes):
+        bank.params[i].copy_(torch.from_numpy(inputs.param(s, i)))
+        bank.grads[i].copy_(torch.from_numpy(inputs.grad(s, i, step=rank)))
+    for i in bank.owned():
+        bank.bufs[i].copy_(torch.from_numpy(inputs.buffer(shapes[i], i)))
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        bank.step(lr=LR, momentum=MU, nesterov=True, ns_steps=NS_STEPS)
+
+    def barrier():
+        torch.cuda.synchronize(device)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(device)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, device)
+    muon.muon_set_debug("record_kernel_events", 1)
+    muon.muon_kernel_times()
+    for _ in range(args.steps):
+        step()
+    barrier()
+    ktimes = muon.muon_kernel_times()
+    muon.muon_set_debug("record_kernel_events", 0)
+    # e2e: this rank's gradients in from pinned host memory, the gathered
+    # parameters out, every step (serialised with the step)
+    g_host = [f.cpu().pin_memory() for f in bank.grad_flat]
+    p_host = [torch.empty(f.shape, dtype=f.dtype).pin_memory() for f in bank.param_flat]
+    e_steps = max(3, args.steps // 4)
+    barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(e_steps):
+        for dst, src in zip(bank.grad_flat, g_host):
+            dst.copy_(src, non_blocking=True)
+        step()
+        for dst, src in zip(p_host, bank.param_flat):
+            dst.copy_(src, non_blocking=True)
+    f1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1) / e_steps, world, device)
+    if bank.workspace is not None and muon.muon_device_status(bank.workspace) != 0:
+        raise RuntimeError("device status after the sharded step")
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+    dist.destroy_process_group()
+    peaks, peak_src = load_peaks()
+    mine = [shapes[i] for i in bank.owned()]
+    kern = kernel_report(ktimes, args.steps, ns_flops(mine), ns_flops_issued(mine), hbm_bytes(mine, 2), peaks)
+    dom = max(kern, key=lambda k: kern[k]["share"])
+    d = kern[dom]
+    n_total = len(shapes)
+    line = {
+        "metric": "muon_step_matrices_per_s", "value": n_total / (ms * 1e-3), "unit": "matrices/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC[args.workload], "matrices": n_total,
+                   "params": int(sum(r * c for r, c in shapes)), "ns_steps": NS_STEPS, "lr": LR, "momentum": MU,
+                   "nesterov": True, "l2": "no flush: the bank's state exceeds the 129 MB L2",
+                   "parallelism": f"data-parallel over {world} ranks: {world} copies of the bank, matrices owned by "
+                                  "work-balanced partition; per size group a bf16 reduce-scatter of the gradients, "
+                                  "the owners' Muon steps, an asynchronous all-gather of the parameters",
+                   "exchange_bytes_per_rank_per_step": bank.exchange_bytes()},
+        "roofline": {"kernel": dom, "bound": d["bound"], "achieved": d["achieved"], "peak": d["peak"],
+                     "unit": d["unit"], "frac": d["frac"], "traffic": None,
+                     "peak_source": f"{peak_src} ({'bf16_tflops burst' if d['unit'] == 'TFLOP/s' else 'hbm_gbs'})"},
+        "kernels": kern,
+        "e2e": {"value": n_total / (e2e_ms * 1e-3), "unit": "matrices/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": int(sum(f.numel() * f.element_size() for f in bank.grad_flat)),
+                "d2h_bytes_per_step": int(sum(f.numel() * f.element_size() for f in bank.param_flat)),
+                "method": "every step uploads this rank's gradients from pinned host memory and reads the gathered "
+                          "parameters back, serialised with the step"},
+        "gpu_launches": int(sum(c for _, c in ktimes.values())),
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
 
 
 def run_adam(args, rank, world, device):
@@ -876,6 +1077,41 @@ def run_fp8(args, rank, world, device):
     barrier()
     kt = muon.muon_kernel_times()
     muon.muon_set_debug("record_kernel_events", 0)
+    # backward (fp8_mm_backward): a seeded bf16 output gradient of M x N,
+    # the forward's E4M3 operands, grad_s filling E5M2
+    gen = torch.Generator(device=device).manual_seed(1234 + rank)
+    Gd = (torch.randn((M, N), generator=gen, device=device) * 1e-3).to(torch.bfloat16)
+    grad_s = float(Gd.abs().max().float().item() / 57344.0 * 1.05)
+    GX = torch.empty((M, K), dtype=torch.bfloat16, device=device)
+    GW = torch.empty((N, K), dtype=torch.bfloat16, device=device)
+    GQ = torch.empty((M, N), dtype=torch.uint8, device=device)
+    bws = muon.new_workspace(muon.fp8_mm_backward_workspace_size(M, N, K), device)
+
+    def bstep():
+        muon.fp8_mm_backward(Gd, XQ, WQ, x_s, w_s, grad_s, grad_x=GX, grad_w=GW, g_f8=GQ, workspace=bws,
+                             stream=stream)
+
+    for _ in range(args.warmup):
+        bstep()
+    barrier()
+    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    b0.record(stream)
+    for _ in range(args.steps):
+        bstep()
+    b1.record(stream)
+    barrier()
+    bms = max_over_ranks(b0.elapsed_time(b1) / args.steps, world, device)
+    muon.muon_set_debug("record_kernel_events", 1)
+    muon.muon_kernel_times()
+    for _ in range(args.steps):
+        bstep()
+    barrier()
+    bkt = muon.muon_kernel_times()
+    muon.muon_set_debug("record_kernel_events", 0)
+    if muon.muon_device_status(bws) != 0:
+        raise RuntimeError("device status after the FP8 backward")
+    del Gd, GX, GW, GQ, bws
+
     # e2e: x and w in from pinned host memory, out back
     in_host = [[X.cpu().pin_memory(), W.cpu().pin_memory()]]
     bufs = [[X, W], [torch.empty_like(X), torch.empty_like(W)]]
@@ -924,6 +1160,27 @@ def run_fp8(args, rank, world, device):
         "gpu_launches": 2 * args.steps,
         "clocks": clk,
     }
+    bflops = 4.0 * M * N * K  # grad_x and grad_w
+    t_ms, t_n = bkt["fp8_transpose"]
+    g_ms2, g_n2 = bkt["fp8_mm_bwd"]
+    r_ms, r_n = bkt["fp8_reduce"]
+    t_bytes = 4.0 * M * N + 2.0 * M * K + 2.0 * N * K  # g r (2) + g_f8 w + g_f8^T w; x_f8, w_f8 r + copies w
+    bk = {"fp8_transpose": {"avg_ms": t_ms / t_n, "achieved": t_bytes / (t_ms / t_n * 1e-3) / 1e9, "unit": "GB/s",
+                            "bound": "hbm", "peak": peaks["hbm_gbs"],
+                            "frac": t_bytes / (t_ms / t_n * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                            "work_per_launch": t_bytes},
+          "fp8_mm_bwd": {"avg_ms": g_ms2 / g_n2, "achieved": bflops / (g_ms2 / g_n2 * 1e-3) / 1e12,
+                         "unit": "TFLOP/s", "bound": "tensor", "peak": fp8_peak,
+                         "frac": bflops / (g_ms2 / g_n2 * 1e-3) / 1e12 / fp8_peak, "work_per_launch": bflops}}
+    if r_n:
+        r_bytes = 4.0 * N * K * 2 + 2.0 * N * K  # two fp32 slices read, bf16 written
+        bk["fp8_reduce"] = {"avg_ms": r_ms / r_n, "achieved": r_bytes / (r_ms / r_n * 1e-3) / 1e9, "unit": "GB/s",
+                            "bound": "hbm", "peak": peaks["hbm_gbs"],
+                            "frac": r_bytes / (r_ms / r_n * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+    line["backward"] = {"what": "fp8_mm_backward: g 65536x3072 bf16 -> E5M2, grad_x = g_f8 . w_f8 and "
+                                "grad_w = g_f8^T . x_f8 on the tensor cores (E5M2 x E4M3), bf16 out",
+                        "ms_per_call": bms, "tflops": bflops * world / (bms * 1e-3) / 1e12, "grad_s": grad_s,
+                        "kernels": bk, "gpu_launches_per_call": 2 + (1 if r_n else 0)}
     if world == 1 and not args.no_cpu_baseline:
         f_cpu, t_cpu = fp8_oracle_sample(args.cpu_budget)
         line["cpu_baseline"] = {"value": f_cpu / t_cpu / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(),

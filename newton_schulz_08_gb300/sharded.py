@@ -1,22 +1,32 @@
 """The Muon step sharded over data-parallel ranks (one process per GPU).
 
-Every rank holds the whole bank of parameters and its own gradients.  Each
-matrix's step depends on that matrix alone, so ownership splits the work
-(muon_partition: heaviest first, identical shapes together, least-loaded
-rank):
+Every rank holds the whole bank of parameters and computes gradients for all
+of it.  Each matrix's step depends on that matrix alone, so ownership splits
+the work (muon_partition: heaviest first, identical shapes together,
+least-loaded rank).  The exchange around the local step follows the page
+"深入解析KellerJordan/modded-nanogpt中的训练架构与优化技术" (reposource.net),
+section "Muon优化器：动量正交化技术" (parameters grouped by size; each rank
+orthogonalises its share of a group; the updated parameters are gathered
+with an asynchronous all_gather_into_tensor, the next group's work
+overlapping it), with a reduce-scatter of the gradients in front, as the
+energy-efficiency page (bxzpzcl.cn) describes for the gradients:
 
-  1. the gradients of each matrix are averaged onto its owner rank (one
-     packed fp32 reduce per owner);
-  2. every rank runs the Muon step (muon_step, the CUDA path) on the matrices
-     it owns; momentum buffers live on the owner only;
-  3. every owner broadcasts its updated parameters (one packed broadcast per
-     owner), so all ranks end with the same parameters.
+  per size group g (largest matrices first):
+    1. reduce_scatter_tensor of the group's gradients, in their own dtype:
+       each rank receives the sum over ranks of the gradients of the
+       matrices it owns, and divides it by the world size (the average);
+    2. muon_step (the CUDA path) on the rank's matrices of the group; their
+       momentum buffers live on the owner only;
+    3. all_gather_into_tensor of the group's updated parameters, issued
+       asynchronously so that it overlaps the next group's steps 1-2.
 
-This is the exchange around the step in the page "深入解析KellerJordan/
-modded-nanogpt中的训练架构与优化技术" (reposource.net), section "Muon优化器：
-动量正交化技术": each rank orthogonalises its share of the parameters and
-the updates are then gathered on all ranks.  The collectives use
-torch.distributed (NCCL for CUDA tensors).
+Layout (what makes the exchange copy-free): for every group the parameters
+and the gradients live in one flat buffer each, ordered by owner rank, every
+rank's segment padded to the group's longest segment.  A rank's segment of
+the gradient buffer is exactly the reduce-scatter's input chunk for that
+rank, and its segment of the parameter buffer is its all-gather input.
+``ShardedBank.params`` and ``ShardedBank.grads`` are views into these
+buffers, in bank order, for the training code to read and write.
 """
 
 import torch
@@ -30,65 +40,117 @@ def owners(shapes, world):
     return muon.partition([tuple(s) for s in shapes], world)
 
 
-def _packed(tensors, dtype):
-    return torch.cat([t.reshape(-1).to(dtype) for t in tensors]) if tensors else None
+def size_groups(shapes):
+    """Matrix indices grouped by element count, largest first (the page
+    groups its parameters by size); bank order within a group."""
+    by = {}
+    for i, (r, c) in enumerate(shapes):
+        by.setdefault(r * c, []).append(i)
+    return [by[k] for k in sorted(by, reverse=True)]
 
 
-def _unpack_into(flat, tensors):
-    off = 0
-    for t in tensors:
-        n = t.numel()
-        t.copy_(flat[off:off + n].view(t.shape).to(t.dtype))
-        off += n
+class _Group:
+    """One size group's owner-ordered layout on one rank."""
+
+    def __init__(self, idx, shapes, owner, world):
+        self.idx = idx
+        self.numel = shapes[idx[0]][0] * shapes[idx[0]][1]
+        self.members = [[i for i in idx if owner[i] == r] for r in range(world)]
+        self.seg = self.numel * max(len(m) for m in self.members)  # elements per rank segment
+        # element offset of each matrix in the flat buffer
+        self.offset = {}
+        for r, mem in enumerate(self.members):
+            for k, i in enumerate(mem):
+                self.offset[i] = r * self.seg + k * self.numel
 
 
-def reduce_grads_to_owners(grads, owner, rank, world, group=None):
-    """Averages every matrix's gradient over the ranks onto its owner.
-    Returns {matrix index: averaged fp32 gradient} for the matrices `rank`
-    owns (new tensors; `grads` is not modified)."""
-    out = {}
-    for r in range(world):
-        idx = [i for i, o in enumerate(owner) if o == r]
-        if not idx:
-            continue
-        flat = _packed([grads[i] for i in idx], torch.float32)
-        dist.reduce(flat, dst=r, op=dist.ReduceOp.SUM, group=group)
-        if r == rank:
-            flat.div_(world)
-            off = 0
-            for i in idx:
-                n = grads[i].numel()
-                out[i] = flat[off:off + n].view(grads[i].shape)
-                off += n
-    return out
+class ShardedBank:
+    """A bank of 2-D matrices stepped with Muon over `world` data-parallel
+    ranks.
 
+    shapes      (rows, cols) of every matrix, identical on every rank;
+    device      where the buffers live (CUDA for the real step; the CPU
+                tests use gloo on CPU tensors);
+    grad_dtype  dtype of the gradients and of the reduce-scatter
+                (bfloat16 by default, as the training computes them).
 
-def broadcast_params_from_owners(params, owner, world, group=None):
-    """Every owner sends its matrices' parameters to all ranks (in place)."""
-    for r in range(world):
-        idx = [i for i, o in enumerate(owner) if o == r]
-        if not idx:
-            continue
-        flat = _packed([params[i] for i in idx], params[idx[0]].dtype)
-        dist.broadcast(flat, src=r, group=group)
-        _unpack_into(flat, [params[i] for i in idx])
+    params (fp32) and grads are lists of views in bank order.  bufs holds a
+    zero-initialised fp32 momentum buffer for each matrix this rank owns
+    (None for the others).  step() runs the exchange and the local steps;
+    `local_step(params, grads, bufs, lr, momentum, nesterov, ns_steps,
+    workspace)` defaults to the CUDA muon_step."""
 
+    def __init__(self, shapes, device, group=None, grad_dtype=torch.bfloat16):
+        self.shapes = [tuple(int(x) for x in s) for s in shapes]
+        self.group = group
+        self.world = dist.get_world_size(group)
+        self.rank = dist.get_rank(group)
+        self.device = torch.device(device)
+        self.owner = owners(self.shapes, self.world)
+        self.groups = [_Group(idx, self.shapes, self.owner, self.world) for idx in size_groups(self.shapes)]
+        self.param_flat = [torch.zeros(self.world * g.seg, dtype=torch.float32, device=self.device)
+                           for g in self.groups]
+        self.grad_flat = [torch.zeros(self.world * g.seg, dtype=grad_dtype, device=self.device) for g in self.groups]
+        # the reduce-scatter's output: this rank's summed (then averaged) gradients
+        self.grad_mine = [torch.empty(g.seg, dtype=grad_dtype, device=self.device) for g in self.groups]
+        self.params = [None] * len(self.shapes)
+        self.grads = [None] * len(self.shapes)
+        self.bufs = [None] * len(self.shapes)
+        self._mine = []  # per group: (index, param view, averaged-gradient view, buffer)
+        for g, pf, gf, gm in zip(self.groups, self.param_flat, self.grad_flat, self.grad_mine):
+            mine = []
+            for i in g.idx:
+                r, c = self.shapes[i]
+                o = g.offset[i]
+                self.params[i] = pf[o:o + r * c].view(r, c)
+                self.grads[i] = gf[o:o + r * c].view(r, c)
+                if self.owner[i] == self.rank:
+                    lo = o - self.rank * g.seg
+                    self.bufs[i] = torch.zeros((r, c), dtype=torch.float32, device=self.device)
+                    mine.append((i, self.params[i], gm[lo:lo + r * c].view(r, c), self.bufs[i]))
+            self._mine.append(mine)
+        self.workspace = None
 
-def sharded_muon_step(params, grads, bufs, lr=0.02, momentum=0.95, nesterov=True, ns_steps=5, group=None,
-                      workspace=None, stream=None):
-    """One data-parallel Muon step.  params, grads, bufs: lists of 2-D CUDA
-    tensors of the whole bank (fp32 params and buffers; bufs are used and
-    updated only for the matrices this rank owns).  Returns the workspace
-    used for the local step (reuse it across steps), or None when this rank
-    owns no matrix."""
-    world = dist.get_world_size(group)
-    rank = dist.get_rank(group)
-    owner = owners([p.shape for p in params], world)
-    mine = reduce_grads_to_owners(grads, owner, rank, world, group)
-    if mine:
-        idx = sorted(mine)
-        workspace = muon.muon_step([params[i] for i in idx], [mine[i] for i in idx], [bufs[i] for i in idx],
-                                   lr=lr, momentum=momentum, nesterov=nesterov, ns_steps=ns_steps,
-                                   workspace=workspace, stream=stream)
-    broadcast_params_from_owners(params, owner, world, group)
-    return workspace if mine else None
+    def owned(self):
+        """Indices of the matrices this rank owns."""
+        return [i for i, o in enumerate(self.owner) if o == self.rank]
+
+    def exchange_bytes(self):
+        """Bytes this rank sends per step: its reduce-scatter input minus its
+        own segment, and its all-gather segment to every other rank (both
+        per group, padding included)."""
+        out = 0
+        for g, gf, pf in zip(self.groups, self.grad_flat, self.param_flat):
+            out += (self.world - 1) * g.seg * (gf.element_size() + pf.element_size())
+        return out
+
+    def step(self, lr=0.02, momentum=0.95, nesterov=True, ns_steps=5, local_step=None, stream=None):
+        """One data-parallel Muon step over the bank (in place)."""
+        if local_step is None:
+            local_step = self._cuda_step
+        pending = []
+        # every group's reduce-scatter is issued up front; each group then
+        # waits for its own before stepping
+        rs = [dist.reduce_scatter_tensor(gm, gf, op=dist.ReduceOp.SUM, group=self.group, async_op=True)
+              for gm, gf in zip(self.grad_mine, self.grad_flat)]
+        for g, mine, work, gm, pf in zip(self.groups, self._mine, rs, self.grad_mine, self.param_flat):
+            work.wait()
+            if mine:
+                gm.div_(self.world)
+                local_step([m[1] for m in mine], [m[2] for m in mine], [m[3] for m in mine], lr, momentum,
+                           nesterov, ns_steps, stream)
+            seg = pf[self.rank * g.seg:(self.rank + 1) * g.seg]
+            pending.append(dist.all_gather_into_tensor(pf, seg, group=self.group, async_op=True))
+        for w in pending:
+            w.wait()
+
+    def _cuda_step(self, params, grads, bufs, lr, momentum, nesterov, ns_steps, stream):
+        # one workspace, sized for the largest group, reused by every group's
+        # call (stream-ordered)
+        need = muon.muon_workspace_size([tuple(p.shape) for p in params])
+        if self.workspace is None or self.workspace.numel() < need:
+            self.workspace = muon.new_workspace(max(need, max(
+                muon.muon_workspace_size([tuple(self.shapes[m[0]]) for m in mine]) for mine in self._mine if mine)),
+                self.device)
+        muon.muon_step(params, grads, bufs, lr=lr, momentum=momentum, nesterov=nesterov, ns_steps=ns_steps,
+                       workspace=self.workspace, stream=stream)

@@ -1,10 +1,11 @@
 """The step on several processes: the work-balanced partition of a bank
 (muon_partition, host only), the way bench.py splits a world-sized bank and
 aggregates its timing, and the exchange of the sharded data-parallel step
-(gradients averaged onto owners, parameters broadcast from owners).  The
-multi-rank tests run two `gloo` ranks on CPU as child processes, each
-computing its own matrices with the oracle standing in for the GPU step; one
-GPU test runs sharded_muon_step itself over a one-rank NCCL group.
+(ShardedBank: reduce-scatter of the gradients by size group, the owners'
+steps, all-gather of the parameters).  The multi-rank tests run two `gloo`
+ranks on CPU as child processes, each computing its own matrices with the
+oracle standing in for the GPU step; one GPU test runs ShardedBank itself
+over a one-rank NCCL group.
 
 The page "深入解析KellerJordan/modded-nanogpt中的训练架构与优化技术"
 (reposource.net), section "Muon优化器：动量正交化技术", shards the step by
@@ -149,30 +150,56 @@ def test_two_gloo_ranks_share_a_world_sized_bank(L):
 
 
 # ------------------------------------------------ sharded data-parallel step
+# several size groups (the 960-element group mixes a tall and a wide shape),
+# uneven ownership within groups, tall, wide and square matrices
+SHARD_BANK = [(24, 40), (24, 40), (40, 24), (24, 40), (32, 32), (32, 32), (16, 48), (20, 20), (20, 20), (20, 20),
+              (8, 56)]
+SHARD_STEPS = 2
+HP = dict(lr=0.02, momentum=0.95, nesterov=True, ns_steps=5)
+
+
+def _grad(shape, i, step, rank):
+    from newton_schulz_08_gb300 import inputs
+    return inputs.grad(shape, i, step=2 * step + rank)
+
+
+def _oracle_local_step(params, grads, bufs, lr, momentum, nesterov, ns_steps, stream):
+    """The owner's step with the oracle standing in for the CUDA path: fp32
+    state in and out, the step in fp64."""
+    import torch
+
+    from oracle import muon_step
+    for p, g, b in zip(params, grads, bufs):
+        new_p, new_b, _ = muon_step(p.numpy().astype(np.float64), g.float().numpy().astype(np.float64),
+                                    b.numpy().astype(np.float64), lr, momentum, nesterov, ns_steps, "fp64")
+        p.copy_(torch.from_numpy(new_p.astype(np.float32)))
+        b.copy_(torch.from_numpy(new_b.astype(np.float32)))
+
+
 def _sharded_worker(rank, world, port, out_dir):
-    """The exchange of sharded_muon_step around the local step, on CPU
-    tensors: gradients averaged onto owners, the owner's step (the oracle
-    stands in for the CUDA step here), parameters broadcast from owners."""
+    """ShardedBank.step on CPU tensors over gloo: reduce-scatter of the bf16
+    gradients, the owners' steps (the oracle stands in for the CUDA step),
+    asynchronous all-gather of the parameters."""
     import torch
     import torch.distributed as dist
 
     from newton_schulz_08_gb300 import inputs, sharded
-    from oracle import muon_step
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
-        params = [torch.from_numpy(inputs.param(s, i)) for i, s in enumerate(SMALL_BANK)]
-        grads = [torch.from_numpy(inputs.grad(s, i, step=rank)) for i, s in enumerate(SMALL_BANK)]
-        bufs = [torch.from_numpy(inputs.buffer(s, i)) for i, s in enumerate(SMALL_BANK)]
-        owner = sharded.owners([p.shape for p in params], world)
-        mine = sharded.reduce_grads_to_owners(grads, owner, rank, world)
-        assert sorted(mine) == [i for i, o in enumerate(owner) if o == rank]
-        for i, g in mine.items():
-            new_p, _, _ = muon_step(params[i].numpy(), g.numpy(), bufs[i].numpy(), 0.02, 0.95, True, 5, "fp64")
-            params[i].copy_(torch.from_numpy(new_p.astype(np.float32)))
-        sharded.broadcast_params_from_owners(params, owner, world)
-        np.save(os.path.join(out_dir, f"p{rank}.npy"), np.concatenate([p.numpy().ravel() for p in params]))
+        bank = sharded.ShardedBank(SHARD_BANK, "cpu")
+        for i, s in enumerate(SHARD_BANK):
+            bank.params[i].copy_(torch.from_numpy(inputs.param(s, i)))
+        for step in range(SHARD_STEPS):
+            for i, s in enumerate(SHARD_BANK):
+                bank.grads[i].copy_(torch.from_numpy(_grad(s, i, step, rank)))
+            bank.step(local_step=_oracle_local_step, **HP)
+        np.save(os.path.join(out_dir, f"p{rank}.npy"), np.concatenate([p.numpy().ravel() for p in bank.params]))
+        np.save(os.path.join(out_dir, f"owned{rank}.npy"), np.array(bank.owned()))
+        for i in bank.owned():
+            np.save(os.path.join(out_dir, f"buf{i}.npy"), bank.bufs[i].numpy())
+        assert all(bank.bufs[i] is None for i in range(len(SHARD_BANK)) if i not in bank.owned())
     finally:
         dist.destroy_process_group()
 
@@ -180,45 +207,85 @@ def _sharded_worker(rank, world, port, out_dir):
 def test_sharded_step_exchange_on_two_gloo_ranks(L):
     import torch.multiprocessing as mp
 
-    from newton_schulz_08_gb300 import inputs
-    from oracle import muon_step
+    import oracle
+    from newton_schulz_08_gb300 import inputs, sharded
     with tempfile.TemporaryDirectory() as d:
         mp.spawn(_sharded_worker, args=(WORKERS, _free_port(), d), nprocs=WORKERS, join=True)
         got = [np.load(os.path.join(d, f"p{r}.npy")) for r in range(WORKERS)]
+        owned = [np.load(os.path.join(d, f"owned{r}.npy")).tolist() for r in range(WORKERS)]
+        bufs = {i: np.load(os.path.join(d, f"buf{i}.npy")) for r in owned for i in r}
+    # every matrix has exactly one owner, and the groups are uneven
+    assert sorted(owned[0] + owned[1]) == list(range(len(SHARD_BANK)))
+    own = sharded.owners(SHARD_BANK, WORKERS)
+    groups = [sharded._Group(idx, SHARD_BANK, own, WORKERS) for idx in sharded.size_groups(SHARD_BANK)]
+    assert any(len(g.members[0]) != len(g.members[1]) for g in groups)
     # every rank ends with the same parameters ...
     np.testing.assert_array_equal(got[0], got[1])
-    # ... equal to one process stepping every matrix with the averaged gradient
-    ref = []
-    for i, s in enumerate(SMALL_BANK):
-        g = (inputs.grad(s, i, step=0) + inputs.grad(s, i, step=1)) / np.float32(WORKERS)
-        new_p, _, _ = muon_step(inputs.param(s, i), g, inputs.buffer(s, i), 0.02, 0.95, True, 5, "fp64")
-        ref.append(new_p.astype(np.float32).ravel())
-    np.testing.assert_array_equal(got[0], np.concatenate(ref))
+    # ... equal, bit for bit, to one process stepping every matrix with the
+    # average of the ranks' bf16 gradients: their bf16 sum (one rounding for
+    # two terms) halved (exact)
+    ref_p, ref_b = [], {}
+    for i, s in enumerate(SHARD_BANK):
+        p, b = inputs.param(s, i), np.zeros(s, np.float32)
+        for step in range(SHARD_STEPS):
+            gs = [oracle.round_to_bf16(_grad(s, i, step, r)) for r in range(WORKERS)]
+            g = oracle.round_to_bf16(gs[0] + gs[1]) / WORKERS
+            new_p, new_b, _ = oracle.muon_step(p.astype(np.float64), g, b.astype(np.float64), HP["lr"],
+                                               HP["momentum"], HP["nesterov"], HP["ns_steps"], "fp64")
+            p, b = new_p.astype(np.float32), new_b.astype(np.float32)
+        ref_p.append(p.ravel())
+        ref_b[i] = b
+    np.testing.assert_array_equal(got[0], np.concatenate(ref_p))
+    for i, b in bufs.items():
+        np.testing.assert_array_equal(b, ref_b[i])
+
+
+def test_sharded_layout_is_owner_ordered_and_padded(L):
+    """The flat buffers hold each rank's matrices in one segment per group,
+    every segment padded to the group's longest."""
+    from newton_schulz_08_gb300 import sharded
+    groups = sharded.size_groups(SHARD_BANK)
+    assert [SHARD_BANK[g[0]][0] * SHARD_BANK[g[0]][1] for g in groups] == [1024, 960, 768, 448, 400]
+    owner = sharded.owners(SHARD_BANK, 3)
+    for idx in groups:
+        g = sharded._Group(idx, SHARD_BANK, owner, 3)
+        assert g.seg == g.numel * max(len(m) for m in g.members)
+        seen = set()
+        for r, mem in enumerate(g.members):
+            for k, i in enumerate(mem):
+                assert owner[i] == r and g.offset[i] == r * g.seg + k * g.numel
+                seen.add(i)
+        assert seen == set(idx)
 
 
 @pytest.mark.gpu
 def test_sharded_step_on_one_nccl_rank_equals_muon_step():
-    """sharded_muon_step with world size 1: the fp32-averaged gradient has the
-    bf16 gradient's values, so the result equals muon_step bit for bit."""
+    """ShardedBank.step with world size 1 (the reduce-scatter and the
+    all-gather are copies): equal to muon_step bit for bit over two steps."""
     import torch
     import torch.distributed as dist
 
     from newton_schulz_08_gb300 import inputs, sharded
-    shapes = [(256, 256), (300, 100), (100, 300), (768, 768)]
+    shapes = [(256, 256), (300, 100), (100, 300), (768, 768), (768, 768)]
     dev = torch.device("cuda")
-    mk = lambda f: [torch.from_numpy(f(s, i)).to(dev) for i, s in enumerate(shapes)]
-    P1, B1 = mk(inputs.param), mk(inputs.buffer)
-    P2, B2 = [p.clone() for p in P1], [b.clone() for b in B1]
-    G = [g.to(torch.bfloat16) for g in mk(inputs.grad)]
+    P2 = [torch.from_numpy(inputs.param(s, i)).to(dev) for i, s in enumerate(shapes)]
+    B2 = [torch.zeros(s, device=dev) for s in shapes]
     store = dist.TCPStore("127.0.0.1", _free_port(), 1, True)
     dist.init_process_group("nccl", store=store, rank=0, world_size=1)
     try:
-        ws = sharded.sharded_muon_step(P1, G, B1)
+        bank = sharded.ShardedBank(shapes, dev)
+        for i, p in enumerate(P2):
+            bank.params[i].copy_(p)
+        for step in range(2):
+            G = [torch.from_numpy(inputs.grad(s, i, step=step)).to(dev).to(torch.bfloat16)
+                 for i, s in enumerate(shapes)]
+            for i, g in enumerate(G):
+                bank.grads[i].copy_(g)
+            bank.step()
+            muon.muon_step(P2, G, B2)
         torch.cuda.synchronize()
-        assert muon.muon_device_status(ws) == muon.MUON_OK
+        assert muon.muon_device_status(bank.workspace) == muon.MUON_OK
     finally:
         dist.destroy_process_group()
-    muon.muon_step(P2, G, B2)
-    torch.cuda.synchronize()
-    for a, b in zip(P1 + B1, P2 + B2):
-        assert torch.equal(a, b)
+    for i in range(len(shapes)):
+        assert torch.equal(bank.params[i], P2[i]) and torch.equal(bank.bufs[i], B2[i])
