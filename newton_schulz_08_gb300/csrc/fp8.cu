@@ -96,6 +96,29 @@ __device__ __forceinline__ uint32_t to_e5m2(float v) {
 __device__ __forceinline__ float word_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float word_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// The two bf16 quotients of a pair (lo, hi): when both take the fast path
+// they are rounded by one paired conversion.
+__device__ __forceinline__ float2 div2_to_bf16(float x0, float x1, float s, float inv) {
+  const float q0 = x0 * inv, q1 = x1 * inv;
+  const uint32_t l0 = __float_as_uint(q0) & 0xFFFFu, l1 = __float_as_uint(q1) & 0xFFFFu;
+  if (isfinite(q0) && isfinite(q1) && l0 - 0x7FFDu > 6u && l1 - 0x7FFDu > 6u)
+    return __bfloat1622float2(__floats2bfloat162_rn(q0, q1));
+  return make_float2(div_to_bf16(x0, s, inv), div_to_bf16(x1, s, inv));
+}
+
+// Two codes (a in the low byte): in range, one paired conversion.
+template <bool E5M2>
+__device__ __forceinline__ uint32_t to_fp8x2(float a, float b) {
+  if (E5M2) {
+    if (fabsf(a) < 61440.0f && fabsf(b) < 61440.0f)
+      return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E5M2));
+    return to_e5m2(a) | (to_e5m2(b) << 8);
+  }
+  if (fabsf(a) <= 464.0f && fabsf(b) <= 464.0f)
+    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+  return to_e4m3(a) | (to_e4m3(b) << 8);
+}
+
 // Four bf16 pairs (one 16-byte vector) to 8 one-byte codes (two words).
 template <bool E5M2>
 __device__ __forceinline__ uint2 quantise8(uint4 w, float s, float inv) {
@@ -103,9 +126,8 @@ __device__ __forceinline__ uint2 quantise8(uint4 w, float s, float inv) {
   uint32_t out[2] = {0u, 0u};
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const float a = div_to_bf16(word_lo(ws[k]), s, inv), b = div_to_bf16(word_hi(ws[k]), s, inv);
-    const uint32_t pair = E5M2 ? (to_e5m2(a) | (to_e5m2(b) << 8)) : (to_e4m3(a) | (to_e4m3(b) << 8));
-    out[k >> 1] |= pair << (16 * (k & 1));
+    const float2 q = div2_to_bf16(word_lo(ws[k]), word_hi(ws[k]), s, inv);
+    out[k >> 1] |= to_fp8x2<E5M2>(q.x, q.y) << (16 * (k & 1));
   }
   return make_uint2(out[0], out[1]);
 }
@@ -149,13 +171,16 @@ cudaError_t launch_fp8_quantize(const Fp8QuantParams& P, int blocks, cudaStream_
 // One 128 x 128 tile of a job per block.  Load: 4 passes of 32 rows, 8
 // threads per row, 16 columns (32 bytes of bf16 or 16 codes) each; a
 // quantising job also writes its 16 codes row-major.  The codes go to a
-// shared tile (row pitch 132 bytes), then each thread reads a 16-row x
-// 4-column block as 16 words, transposes it as four 4 x 4 byte blocks and
-// writes 16 bytes to each of 4 rows of the transposed output.
+// shared tile of 128-byte rows whose 4-byte words are swizzled: word w of
+// row r sits at w ^ (4 * ((r / 16) % 8)).  Then each thread reads a
+// 16-row x 4-column block as 16 words, transposes it as four 4 x 4 byte
+// blocks and writes 16 bytes to each of 4 rows of the transposed output.
+// In a warp the 4 lanes of a group take 4 adjacent word columns and the 8
+// groups the 8 row blocks: the swizzle puts the 32 words of one read in 32
+// different banks, and each store writes 4 whole 128-byte output rows.
 __global__ void __launch_bounds__(kThreads) fp8_transpose_kernel(const __grid_constant__ Fp8TParams P) {
   grid_dep();
-  constexpr int kPitch = kFp8Tile + 4;
-  __shared__ __align__(16) uint8_t tile[kFp8Tile * kPitch];
+  __shared__ __align__(16) uint32_t tile[kFp8Tile * kFp8Tile / 4];
   int j = 0;
   while (j + 1 < P.n_jobs && static_cast<int>(blockIdx.x) >= P.job[j + 1].tile_begin) ++j;
   const Fp8TJob& J = P.job[j];
@@ -163,6 +188,7 @@ __global__ void __launch_bounds__(kThreads) fp8_transpose_kernel(const __grid_co
   const int r0 = (t / J.tiles_c) * kFp8Tile, c0 = (t % J.tiles_c) * kFp8Tile;
   const int tid = threadIdx.x;
   const int cl = (tid & 7) * 16;  // tile columns cl .. cl + 15
+  auto slot = [](int r, int w) { return r * (kFp8Tile / 4) + (w ^ (((r >> 4) & 7) << 2)); };
   // rows and columns are multiples of 16: a 16-element piece is wholly
   // inside the source or wholly outside
   if (J.quant) {
@@ -187,11 +213,7 @@ __global__ void __launch_bounds__(kThreads) fp8_transpose_kernel(const __grid_co
         b = quantise8<true>(v[p][1], J.scale, J.inv_scale);
         *reinterpret_cast<uint4*>(J.dst + static_cast<long long>(r) * J.cols + c) = make_uint4(a.x, a.y, b.x, b.y);
       }
-      uint32_t* row = reinterpret_cast<uint32_t*>(tile + rl * kPitch + cl);
-      row[0] = a.x;
-      row[1] = a.y;
-      row[2] = b.x;
-      row[3] = b.y;
+      *reinterpret_cast<uint4*>(&tile[slot(rl, cl >> 2)]) = make_uint4(a.x, a.y, b.x, b.y);
     }
   } else {
     const uint8_t* src = static_cast<const uint8_t*>(J.src);
@@ -203,26 +225,21 @@ __global__ void __launch_bounds__(kThreads) fp8_transpose_kernel(const __grid_co
       if (r < J.rows && c < J.cols) v[p] = *reinterpret_cast<const uint4*>(src + static_cast<long long>(r) * J.cols + c);
     }
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      uint32_t* row = reinterpret_cast<uint32_t*>(tile + (p * 32 + (tid >> 3)) * kPitch + cl);
-      row[0] = v[p].x;
-      row[1] = v[p].y;
-      row[2] = v[p].z;
-      row[3] = v[p].w;
-    }
+    for (int p = 0; p < 4; ++p) *reinterpret_cast<uint4*>(&tile[slot(p * 32 + (tid >> 3), cl >> 2)]) = v[p];
   }
   __syncthreads();
-  // transposed: output rows c0 + oc .. + 3 (source columns), source rows
+  // transposed: output rows c0 + 4 wc .. + 3 (source columns), source rows
   // r0 + rb .. + 15 as 16 bytes of each
-  const int oc = (tid >> 3) * 4;
-  const int rb = (tid & 7) * 16;
+  const int lane = tid & 31;
+  const int wc = (tid >> 5) * 4 + (lane & 3);
+  const int rb = (lane >> 2) * 16;
   uint32_t o[4][4];  // [output row][word]
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     uint32_t a[4];
 #pragma unroll
-    for (int m = 0; m < 4; ++m) a[m] = *reinterpret_cast<const uint32_t*>(tile + (rb + 4 * k + m) * kPitch + oc);
-    // a[m] byte i = tile[rb + 4k + m][oc + i]; output row i, word k, byte m
+    for (int m = 0; m < 4; ++m) a[m] = tile[slot(rb + 4 * k + m, wc)];
+    // a[m] byte i = tile[rb + 4k + m][4 wc + i]; output row i, word k, byte m
     const uint32_t t0 = __byte_perm(a[0], a[1], 0x5140), t1 = __byte_perm(a[2], a[3], 0x5140);
     const uint32_t t2 = __byte_perm(a[0], a[1], 0x7362), t3 = __byte_perm(a[2], a[3], 0x7362);
     o[0][k] = __byte_perm(t0, t1, 0x5410);
@@ -234,7 +251,7 @@ __global__ void __launch_bounds__(kThreads) fp8_transpose_kernel(const __grid_co
   if (rr < J.rows) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int c = c0 + oc + i;
+      const int c = c0 + 4 * wc + i;
       if (c < J.cols)
         *reinterpret_cast<uint4*>(J.dst_t + static_cast<long long>(c) * J.rows + rr) =
             make_uint4(o[i][0], o[i][1], o[i][2], o[i][3]);

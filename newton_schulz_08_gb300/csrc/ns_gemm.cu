@@ -155,6 +155,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   // the Gram and the FP8 product stage no epilogue input; an FP8 K block is
   // 128 one-byte elements (a 128-byte row, as 64 bf16 are)
   constexpr bool kNoAux = MODE == kGram || MODE == kFp8;
+  // the Gram stages one 64 x 32 box per warp (32 KB in all); the others stage
+  // the warp's two boxes (64 KB)
+  constexpr bool kSmallStg = MODE == kGram;
   constexpr int kKB = MODE == kFp8 ? 2 * kBK : kBK;  // elements per K block
   uint8_t* stg = smem + kSt * kStageBytes;  // epilogue staging tile
   uint64_t* bars = reinterpret_cast<uint64_t*>(stg + GemmShape<MODE>::staging);
@@ -387,7 +390,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       }
     };
     auto store_box = [&](const GemmClass& C, const Tile& tl, int bx) {
-      const int sbx = kNoAux ? colhalf : bx;
+      const int sbx = kSmallStg ? colhalf : bx;
       ptx::tma_store_3d(&C.tmOut, stg_a + sbx * (kBM / 2) * 128 + my_rows, tl.J * kBN + 64 * bx,
                         tl.I * kBM + rowoff + q * kEpiRows, tl.idx);
       ptx::bulk_commit();
@@ -499,25 +502,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         ptx::tmem_ld32(tb + ch * 32, r);
         ptx::tmem_ld_wait();
         // staging box: the tile's 64-column box, or (Gram) the warp's one box
-        const int sbx = kNoAux ? colhalf : (c0 >> 6);
+        const int sbx = kSmallStg ? colhalf : (c0 >> 6);
         const uint32_t rowa = stg_a + sbx * ((kBM / 2) * 128) + row_local * 128;
         if (MODE == kFp8 && C.ksplit > 1) {
           // a slice of a split contraction: the fp32 partial sums of these
           // 32 columns (128 bytes per row) fill the warp's 32 x 128-byte
           // slot as one fp32 box, stored to the slice's plane of the
           // partial-sum array once the previous chunk's box has been read
-          if (ch > 0) {
-            if (lane == 0) ptx::bulk_wait_read0();
+          // (two slots per warp, used in turn: a slot is rewritten once the
+          // store two chunks back has read it)
+          const uint32_t fslot = stg_a + (2 * colhalf + (ch & 1)) * ((kBM / 2) * 128);
+          if (ch > 1) {
+            if (lane == 0) ptx::bulk_wait_read1();
             __syncwarp();
           }
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            ptx::sts128(rowa + ((j ^ (row_local & 7)) << 4), r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+            ptx::sts128(fslot + row_local * 128 + ((j ^ (row_local & 7)) << 4), r[4 * j], r[4 * j + 1], r[4 * j + 2],
+                        r[4 * j + 3]);
           ptx::fence_async_smem();
           __syncwarp();
           if (lane == 0) {
-            ptx::tma_store_3d(&C.tmAux, stg_a + colhalf * ((kBM / 2) * 128) + my_rows, tl.J * kBN + c0,
-                              tl.I * kBM + rowoff + q * kEpiRows, tl.split);
+            ptx::tma_store_3d(&C.tmAux, fslot + my_rows, tl.J * kBN + c0, tl.I * kBM + rowoff + q * kEpiRows,
+                              tl.split);
             ptx::bulk_commit();
           }
           if (ch == 3) {
@@ -527,7 +534,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           }
           continue;
         }
-        if (kNoAux && ch == 2) {
+        if (kSmallStg && ch == 2) {
           // the warp's box still holds its first half until the store has read it
           if (lane == 0) ptx::bulk_wait_read0();
           __syncwarp();

@@ -214,6 +214,8 @@ constexpr int kStageOut = (kBM / 2) * kBN * 2;  // 64 KB epilogue staging
 // staging holds one 64 x 32 box per warp (32 KB, reused for the warp's second
 // box once the first has been stored) and the space freed is a sixth operand
 // stage; the polynomial and update tiles stage the input next to the output.
+// The FP8 product's tiles are short (6 K blocks at K = 768), so its warps
+// stage both their boxes at once and it keeps five stages.
 // Gram / poly: the largest m for which A is stored as its blocks on and above
 // the diagonal only, the polynomial reading the others transposed.  Transposed
 // reads walk 64 rows per K block; for wider matrices their lost locality costs
@@ -223,8 +225,8 @@ constexpr int kSymUpperMaxM = 768;
 
 template <int MODE>
 struct GemmShape {
-  static constexpr int stages = MODE == kGram || MODE == kFp8 ? kStages + 1 : kStages;
-  static constexpr int staging = MODE == kGram || MODE == kFp8 ? kStageOut / 2 : kStageOut;
+  static constexpr int stages = MODE == kGram ? kStages + 1 : kStages;
+  static constexpr int staging = MODE == kGram ? kStageOut / 2 : kStageOut;
   static constexpr int smem = stages * kStageBytes + staging + 1024 /*align*/ + 256 /*barriers*/;
 };
 constexpr int kEpiWarps = 8;     // two warps per TMEM lane quarter, one per column half
