@@ -316,6 +316,20 @@ bool encode_map4(CUtensorMap* map, void* base, int cols, int rows, int count, in
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D fp32 map over one rows x cols row-major matrix, box 32 x 32 with
+// 128-byte swizzle: a parameter matrix streamed by the last update.
+bool encode_map_f32_2d(CUtensorMap* map, void* base, long long cols, long long rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc || g_fail_encode.load()) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // square kBM x kBN tiles on and above the diagonal
 int sym_tiles_per_mat(int m) {
   const int tn = static_cast<int>(ceil_div(m, kBN));
@@ -344,6 +358,7 @@ struct Prepared {
   std::vector<K1Params> k1;
   std::vector<NormParams> norm;
   std::vector<GemmParams> gemm;
+  std::vector<GemmParamsP> gemm_p;  // launches that stream the parameters
   std::vector<ApplyParams> apply;
   std::vector<LaunchRec> seq;
 };
@@ -503,11 +518,28 @@ muon_status_t prepare(const std::vector<JobMat>& mats, const Plan& P, int ns_ste
           // the Muon step's last update applies p -= lr X' itself
           gp.table = table;
           gp.apply = mode == kUpdate && final_mode == kFinalParam && t == ns_steps - 1;
-          const int variant = sym | (gp.apply << 1);
+          // the parameters stream through shared memory as TMA boxes of a
+          // tensor map per matrix, when the maps fit in the kernel's
+          // parameters and every row of every matrix starts 16-byte aligned
+          bool streamed = gp.apply && N <= kMaxPMaps;
+          for (int j = 0; j < ng; ++j) streamed = streamed && gp.cls[j].m % 4 == 0 && gp.cls[j].n % 4 == 0;
+          const int variant = sym + 2 * (gp.apply ? (streamed ? 2 : 1) : 0);
           int pairs = 0;
           if (ns_gemm_pairs(mode, variant, sms, &pairs) != cudaSuccess) return MUON_ERR_CUDA;
-          Q.seq.push_back({kLGemm, gp.apply ? 6 : 2 + mode, pairs, mode, variant, static_cast<int>(Q.gemm.size())});
-          Q.gemm.push_back(gp);
+          if (streamed) {
+            GemmParamsP pp;
+            std::memset(&pp, 0, sizeof(pp));
+            static_cast<GemmParams&>(pp) = gp;
+            for (int k = 0; k < N; ++k) {
+              const JobMat& M = mats[P.order[k]];
+              if (!encode_map_f32_2d(&pp.pmap[k], M.out, M.C, M.R)) return MUON_ERR_CUDA;
+            }
+            Q.seq.push_back({kLGemm, 6, pairs, mode, variant, static_cast<int>(Q.gemm_p.size())});
+            Q.gemm_p.push_back(pp);
+          } else {
+            Q.seq.push_back({kLGemm, gp.apply ? 6 : 2 + mode, pairs, mode, variant, static_cast<int>(Q.gemm.size())});
+            Q.gemm.push_back(gp);
+          }
         }
       }
     }
@@ -563,6 +595,13 @@ muon_status_t enqueue(const Prepared& Q, char* ws, float lr, float mu, int neste
       e = launch_momentum_cast(kp, L.grid, stream);
     } else if (L.type == kLNorm) {
       e = launch_normalise(Q.norm[L.index], L.grid, stream);
+    } else if (L.type == kLGemm && L.variant >= 4) {
+      GemmParamsP gp = Q.gemm_p[L.index];
+      gp.lr = lr;
+      gp.wait_budget = budget;
+      gp.inject_stall = stall;
+      gp.wait_profile = prof;
+      e = launch_ns_gemm(L.mode, L.variant, gp, L.grid, stream);
     } else if (L.type == kLGemm) {
       GemmParams gp = Q.gemm[L.index];
       gp.lr = lr;

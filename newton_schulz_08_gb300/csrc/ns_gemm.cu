@@ -148,10 +148,12 @@ __device__ __forceinline__ float word_hi(uint32_t w) { return __uint_as_float(w 
 // p <- p - lr X' instead of storing X'; also compile-time, so that the other
 // updates run without its registers.
 template <int MODE, int SYM, int APPLY>
-__global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmParams P) {
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    ns_gemm_kernel(const __grid_constant__ typename GemmParamsOf<APPLY>::type P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  constexpr int kSt = GemmShape<MODE>::stages;
+  using Shape = GemmShape<MODE, APPLY>;
+  constexpr int kSt = Shape::stages;
   // the Gram and the FP8 product stage no epilogue input; an FP8 K block is
   // 128 one-byte elements (a 128-byte row, as 64 bf16 are)
   constexpr bool kNoAux = MODE == kGram || MODE == kFp8;
@@ -160,14 +162,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
   constexpr bool kSmallStg = MODE == kGram;
   constexpr int kKB = MODE == kFp8 ? 2 * kBK : kBK;  // elements per K block
   uint8_t* stg = smem + kSt * kStageBytes;  // epilogue staging tile
-  uint64_t* bars = reinterpret_cast<uint64_t*>(stg + GemmShape<MODE>::staging);
+  uint8_t* pslots = stg + Shape::staging;    // APPLY 2: parameter blocks
+  uint64_t* bars = reinterpret_cast<uint64_t*>(pslots + Shape::pslots);
   uint64_t* full = bars;                       // leader: both CTAs' tiles landed
   uint64_t* empty = bars + kSt;            // stage free in this CTA
   uint64_t* tfull = bars + 2 * kSt;        // accumulator ready (this CTA's lanes)
   uint64_t* tempty = bars + 2 * kSt + 2;   // leader: both CTAs drained it
   uint64_t* drain = bars + 2 * kSt + 4;
   uint64_t* aux_full = bars + 2 * kSt + 5; // [kEpiWarps] epilogue input of a warp landed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kSt + 5 + kEpiWarps);
+  uint64_t* pfull = aux_full + kEpiWarps;   // [kEpiWarps][2] APPLY 2: a parameter block landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pfull + 2 * kEpiWarps);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* never = reinterpret_cast<volatile int*>(tmem_slot + 2);  // stays 0
 
@@ -191,6 +195,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
     }
     ptx::mbar_init(ptx::smem_addr(drain), 1);
     for (int w = 0; w < kEpiWarps; ++w) ptx::mbar_init(ptx::smem_addr(&aux_full[w]), 1);
+    for (int w = 0; w < 2 * kEpiWarps; ++w) ptx::mbar_init(ptx::smem_addr(&pfull[w]), 1);
     *abort = 0;
     *never = 0;
     ptx::fence_mbar_init();
@@ -443,6 +448,41 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         }
       }
     };
+    // APPLY 2: the parameter block of chunk ch (32 columns of X') of tile t
+    // moves through slot ch % 2 of this warp as one 32 x 32 fp32 TMA box of
+    // the matrix's own tensor map (128-byte swizzle; clipped or zero-filled
+    // at the matrix edge): p's rows are X' rows (wide and square matrices)
+    // or X' columns (tall ones, p = X'^T).  The block of the next chunk (of
+    // the next tile after a tile's last chunk) is loaded while a chunk is
+    // applied.
+    constexpr bool bulkp = MODE == kUpdate && APPLY == 2;
+    const uint32_t pslot0 = ptx::smem_addr(pslots) + static_cast<uint32_t>((warp - 2) * 2 * kPSlot);
+    uint32_t p_phase[2] = {0u, 0u};
+    bool p_pending[2] = {false, false};
+    // box coordinates (x: column, y: row of p) of a chunk's block
+    auto p_xy = [&](const Tile& tn, int tall, int ch, int* x, int* y) {
+      const int r0 = tn.I * kBM + rowoff + q * kEpiRows;
+      const int c0 = tn.J * kBN + colhalf * (kBN / 2) + ch * 32;
+      *x = tall ? r0 : c0;
+      *y = tall ? c0 : r0;
+    };
+    auto p_map = [&](const GemmClass& Cn, const Tile& tn) -> const CUtensorMap* {
+      if constexpr (APPLY == 2) return &P.pmap[Cn.mat_begin + tn.idx];
+      return nullptr;
+    };
+    auto p_load = [&](int t, int ch, int sl) {  // lane 0
+      const Tile tn = decode_tile<MODE>(P, t);
+      const GemmClass& Cn = P.cls[tn.cls];
+      int x, y;
+      p_xy(tn, P.table[Cn.mat_begin + tn.idx].tall, ch, &x, &y);
+      const uint32_t bar = ptx::smem_addr(&pfull[(warp - 2) * 2 + sl]);
+      ptx::mbar_arrive_expect_tx(bar, kPSlot);
+      ptx::tma_load_2d(pslot0 + sl * kPSlot, p_map(Cn, tn), bar, x, y);
+    };
+    if (bulkp && pair < P.total_tiles) {
+      if (lane == 0) p_load(pair, 0, 0);
+      p_pending[0] = true;
+    }
     if (!kNoAux && lane == 0 && pair < P.total_tiles) load_aux(pair);
     uint32_t aux_phase = 0;
     bool ok = true;
@@ -491,7 +531,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
         float* pc = nullptr;
         const int rt = tl.I * kBM + rowoff + row_local;
         const int ct = tl.J * kBN + c0;
-        if (MODE == kUpdate && fuse && ptall) {
+        if (MODE == kUpdate && fuse && ptall && !bulkp) {
           pc = pm + static_cast<long long>(ct) * C.m + rt;
 #pragma unroll
           for (int j = 0; j < 32; ++j)
@@ -574,7 +614,69 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           }
           if (!(fuse && ptall)) ptx::sts128(addr, wq[0], wq[1], wq[2], wq[3]);
         }
-        if (MODE == kUpdate && fuse && ptall) {
+        if (bulkp) {
+          // the other slot (its last store has read it) takes the next
+          // chunk's block
+          {
+            const int nt = ch < 3 ? t : t + npairs;
+            if (__all_sync(0xFFFFFFFFu, nt < P.total_tiles && !*abort)) {
+              if (lane == 0) {
+                ptx::bulk_wait_read0();
+                p_load(nt, (ch + 1) & 3, (ch + 1) & 1);
+              }
+              p_pending[(ch + 1) & 1] = true;
+              __syncwarp();
+            }
+          }
+          // p <- p - lr X' on this chunk's block in shared memory, then back
+          const int sl = ch & 1;
+          const uint32_t slot = pslot0 + sl * kPSlot;
+          if (ptx::mbar_wait(ptx::smem_addr(&pfull[(warp - 2) * 2 + sl]), p_phase[sl], budget, abort)) {
+            p_phase[sl] ^= 1;
+            p_pending[sl] = false;
+          } else {
+            raise_timeout(P, abort);  // the block may still land: waited for at the end
+          }
+          __syncwarp();  // (wide) every lane's X' row is staged
+          if (!ptall) {
+            // 8 lanes per block row, 4 columns (16 bytes of p, 8 of X') each
+            const int colin = (c0 & 63) + (lane & 7) * 4;  // column within the 64-column box
+            const uint32_t box = stg_a + (c0 >> 6) * ((kBM / 2) * 128);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int br = 4 * k + (lane >> 3);  // block row
+              const int rl = q * kEpiRows + br;
+              uint32_t x0, x1;
+              ptx::lds64(box + rl * 128 + (((colin >> 3) ^ (rl & 7)) << 4) + (colin & 7) * 2, x0, x1);
+              float4 pv4;
+              const uint32_t pa = slot + br * 128 + (((lane & 7) ^ (br & 7)) << 4);
+              ptx::lds128f(pa, pv4);
+              pv4.x = fmaf(-P.lr, word_lo(x0), pv4.x);
+              pv4.y = fmaf(-P.lr, word_hi(x0), pv4.y);
+              pv4.z = fmaf(-P.lr, word_lo(x1), pv4.z);
+              pv4.w = fmaf(-P.lr, word_hi(x1), pv4.w);
+              ptx::sts128f(pa, pv4);
+            }
+          } else {
+            // block row j is X' column c0 + j; this lane's X' row is its column
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const uint32_t pa = slot + j * 128 + (((lane >> 2) ^ (j & 7)) << 4) + (lane & 3) * 4;
+              float pvj;
+              ptx::lds32(pa, pvj);
+              ptx::sts32(pa, fmaf(-P.lr, (j & 1) ? word_hi(ow[j >> 1]) : word_lo(ow[j >> 1]), pvj));
+            }
+          }
+          ptx::fence_async_smem();
+          __syncwarp();
+          if (lane == 0 && !*abort) {
+            int x, y;
+            p_xy(tl, ptall, ch, &x, &y);
+            ptx::tma_store_2d(p_map(C, tl), slot, x, y);
+            ptx::bulk_commit();
+          }
+        }
+        if (MODE == kUpdate && fuse && ptall && !bulkp) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const float o = (j & 1) ? word_hi(ow[j >> 1]) : word_lo(ow[j >> 1]);
@@ -591,7 +693,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
           // this warp's rows of box 2*colhalf + ch/2 are written: store them
           // (or apply them to p)
           if (MODE == kUpdate && fuse) {
-            if (!ptall) apply_box(C, tl, pm, 2 * colhalf + (ch >> 1));
+            if (!ptall && !bulkp) apply_box(C, tl, pm, 2 * colhalf + (ch >> 1));
           } else {
             ptx::fence_async_smem();
             __syncwarp();
@@ -649,6 +751,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
       // an input tile may still be in flight
       ptx::mbar_wait(ptx::smem_addr(my_aux), aux_phase, budget, never);
     }
+    if (bulkp && *abort) {
+      // so may parameter blocks
+#pragma unroll
+      for (int sl = 0; sl < 2; ++sl)
+        if (p_pending[sl] && lane == 0)
+          ptx::mbar_wait(ptx::smem_addr(&pfull[(warp - 2) * 2 + sl]), p_phase[sl], budget, never);
+    }
   }
 
   ptx::tc_fence_before();
@@ -676,6 +785,8 @@ template __global__ void ns_gemm_kernel<kUpdate, 0, 0>(const __grid_constant__ G
 template __global__ void ns_gemm_kernel<kUpdate, 0, 1>(const __grid_constant__ GemmParams P);
 template __global__ void ns_gemm_kernel<kUpdate, 1, 0>(const __grid_constant__ GemmParams P);
 template __global__ void ns_gemm_kernel<kUpdate, 1, 1>(const __grid_constant__ GemmParams P);
+template __global__ void ns_gemm_kernel<kUpdate, 0, 2>(const __grid_constant__ GemmParamsP P);
+template __global__ void ns_gemm_kernel<kUpdate, 1, 2>(const __grid_constant__ GemmParamsP P);
 template __global__ void ns_gemm_kernel<kFp8, 0, 0>(const __grid_constant__ GemmParams P);
 
 // ------------------------------------------------------------------ launcher
@@ -683,7 +794,8 @@ namespace {
 
 // The kernel instantiation of a (mode, variant) and its shared memory.
 // Variant bit 0: A (and B) stored block-upper (Gram, polynomial, update);
-// bit 1: the update with the parameter update.  FP8: 0.
+// variant / 2: the update with the parameter update (1: from registers, 2:
+// streamed through shared memory).  FP8: 0.
 const void* gemm_fn(int mode, int variant, int* smem) {
   switch (mode) {
     case kGram:
@@ -695,12 +807,14 @@ const void* gemm_fn(int mode, int variant, int* smem) {
       return variant & 1 ? reinterpret_cast<const void*>(&ns_gemm_kernel<kPoly, 1, 0>)
                          : reinterpret_cast<const void*>(&ns_gemm_kernel<kPoly, 0, 0>);
     case kUpdate:
-      *smem = GemmShape<kUpdate>::smem;
-      switch (variant & 3) {
+      *smem = variant >= 4 ? GemmShape<kUpdate, 2>::smem : GemmShape<kUpdate>::smem;
+      switch (variant) {
         case 0: return reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate, 0, 0>);
         case 1: return reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate, 1, 0>);
         case 2: return reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate, 0, 1>);
-        default: return reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate, 1, 1>);
+        case 3: return reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate, 1, 1>);
+        case 4: return reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate, 0, 2>);
+        default: return reinterpret_cast<const void*>(&ns_gemm_kernel<kUpdate, 1, 2>);
       }
     default:
       *smem = GemmShape<kFp8>::smem;
@@ -724,7 +838,7 @@ void gemm_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute (&attr)[2], int sm
 }
 
 constexpr int kMaxGemmDevices = 64;
-constexpr int kGemmSlots = 16;  // mode * 4 + variant
+constexpr int kGemmSlots = 32;  // mode * 8 + variant
 std::mutex g_pairs_mu;
 int g_max_pairs[kMaxGemmDevices][kGemmSlots] = {};
 
@@ -739,7 +853,7 @@ cudaError_t ns_gemm_pairs(int mode, int variant, int num_sms, int* pairs) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxGemmDevices) return cudaErrorInvalidDevice;
-  const int slot = mode * 4 + variant;
+  const int slot = mode * 8 + variant;
   std::lock_guard<std::mutex> lk(g_pairs_mu);
   int& n = g_max_pairs[dev][slot];
   if (n <= 0) {

@@ -167,6 +167,24 @@ struct GemmParams {
                                 //   in p's own layout) instead of storing X'
 };
 
+// The Muon step's last update with the parameters streamed through shared
+// memory (APPLY 2): one 2-D fp32 tensor map per matrix of the launch, in
+// class order, over the parameter in its own layout (box 32 x 32, 128-byte
+// swizzle).  Kernel parameters are limited to 32 KB, which bounds the
+// number of matrices; larger banks take the register path.
+constexpr int kMaxPMaps = 190;
+struct GemmParamsP : GemmParams {
+  CUtensorMap pmap[kMaxPMaps];
+};
+template <int APPLY>
+struct GemmParamsOf {
+  using type = GemmParams;
+};
+template <>
+struct GemmParamsOf<2> {
+  using type = GemmParamsP;
+};
+
 // diagnostics counters per CTA (clock64 cycles unless noted)
 enum WaitCounter {
   kWpProducerEmpty = 0,  // producer waiting for a free stage
@@ -223,14 +241,24 @@ constexpr int kStageOut = (kBM / 2) * kBN * 2;  // 64 KB epilogue staging
 // 768-, 1024-, 1600- and 4096-wide banks).
 constexpr int kSymUpperMaxM = 768;
 
-template <int MODE>
-struct GemmShape {
-  static constexpr int stages = MODE == kGram ? kStages + 1 : kStages;
-  static constexpr int staging = MODE == kGram ? kStageOut / 2 : kStageOut;
-  static constexpr int smem = stages * kStageBytes + staging + 1024 /*align*/ + 256 /*barriers*/;
-};
+//
+// The Muon step's last update (APPLY 2) streams the parameters through
+// shared memory: every epilogue warp owns two slots of 32 rows x 32 fp32
+// (4 KB) for the parameter blocks of its next chunks; the operand ring
+// gives up two stages for them (that launch is bound by its 8 bytes of
+// parameter traffic per element, not by the MMAs).
 constexpr int kEpiWarps = 8;     // two warps per TMEM lane quarter, one per column half
 constexpr int kEpiRows = 32;     // rows of an epilogue staging box: one warp's TMEM lane quarter
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
+constexpr int kPSlot = 32 * 32 * 4;  // one parameter block: 32 rows of 128 bytes
+constexpr int kGemmBarBytes = 512;   // mbarriers and flags
+
+template <int MODE, int APPLY = 0>
+struct GemmShape {
+  static constexpr int stages = MODE == kGram ? kStages + 1 : (APPLY == 2 ? kStages - 2 : kStages);
+  static constexpr int staging = MODE == kGram ? kStageOut / 2 : kStageOut;
+  static constexpr int pslots = APPLY == 2 ? kEpiWarps * 2 * kPSlot : 0;
+  static constexpr int smem = stages * kStageBytes + staging + pslots + 1024 /*align*/ + kGemmBarBytes;
+};
 
 }  // namespace muon
