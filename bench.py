@@ -1133,6 +1133,11 @@ def run_fp8(args, rank, world, device):
     peaks, peak_src = load_peaks()
     flops = 2.0 * M * N * K
     fp8_peak = 2.0 * peaks["bf16_tflops"]  # nominal dense FP8 : BF16 rate = 4.5 : 2.25
+    fp8_traffic = {}
+    tfile = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tfile):
+        with open(tfile) as f:
+            fp8_traffic = json.load(f).get("fp8", {})
     g_ms, g_n = kt["fp8_mm"]
     q_ms, q_n = kt["fp8_quantize"]
     g_avg, q_avg = g_ms / g_n, q_ms / q_n
@@ -1147,7 +1152,7 @@ def run_fp8(args, rank, world, device):
                    "l2": "no flush: x (101 MB bf16) and out (403 MB bf16) exceed the 129 MB L2",
                    "parallelism": f"{world} ranks, one product each" if world > 1 else "1 GPU"},
         "roofline": {"kernel": "fp8_mm", "bound": "tensor", "achieved": ach, "peak": fp8_peak, "unit": "TFLOP/s",
-                     "frac": ach / fp8_peak, "traffic": None,
+                     "frac": ach / fp8_peak, "traffic": fp8_traffic.get("fp8_mm"),
                      "peak_source": f"{peak_src} bf16_tflops burst x 2 (nominal FP8 : BF16 dense rate)"},
         "kernels": {"fp8_quantize": {"avg_ms": q_avg, "achieved": q_bytes / (q_avg * 1e-3) / 1e9, "unit": "GB/s",
                                      "bound": "hbm", "peak": peaks["hbm_gbs"],
@@ -1168,7 +1173,7 @@ def run_fp8(args, rank, world, device):
     bk = {"fp8_transpose": {"avg_ms": t_ms / t_n, "achieved": t_bytes / (t_ms / t_n * 1e-3) / 1e9, "unit": "GB/s",
                             "bound": "hbm", "peak": peaks["hbm_gbs"],
                             "frac": t_bytes / (t_ms / t_n * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                            "work_per_launch": t_bytes},
+                            "work_per_launch": t_bytes, "traffic": fp8_traffic.get("fp8_transpose")},
           "fp8_mm_bwd": {"avg_ms": g_ms2 / g_n2, "achieved": bflops / (g_ms2 / g_n2 * 1e-3) / 1e12,
                          "unit": "TFLOP/s", "bound": "tensor", "peak": fp8_peak,
                          "frac": bflops / (g_ms2 / g_n2 * 1e-3) / 1e12 / fp8_peak, "work_per_launch": bflops}}
