@@ -520,6 +520,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       ptx::tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN + colhalf * (kBN / 2);
       uint32_t w[4][16];  // the rounded tile, kept for the mirrored writes
+      // the accumulator's 4 chunks of 32 columns are read one chunk ahead:
+      // chunk ch + 1's TMEM load is in flight while chunk ch is processed
+      // (except in the register-path parameter update, whose registers are
+      // too many to keep a load in flight safely: there each chunk's load is
+      // waited for at once)
+      constexpr bool kPipeTmem = !(MODE == kUpdate && APPLY == 1);
+      uint32_t rbuf[2][32];
+      __syncwarp();
+      if (kPipeTmem) ptx::tmem_ld32(tb, rbuf[0]);
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         const int c0 = colhalf * (kBN / 2) + ch * 32;  // column within the tile
@@ -537,10 +546,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (int j = 0; j < 32; ++j)
             pv[j] = (rt < C.m && ct + j < C.n) ? pc[static_cast<long long>(j) * C.m] : 0.0f;
         }
-        uint32_t r[32];
-        __syncwarp();
-        ptx::tmem_ld32(tb + ch * 32, r);
-        ptx::tmem_ld_wait();
+        uint32_t(&r)[32] = rbuf[ch & 1];
+        if (!kPipeTmem) {
+          __syncwarp();
+          ptx::tmem_ld32(tb + ch * 32, r);
+        }
+        ptx::tmem_ld_wait(r);
+        if (ch == 3) {
+          // every column of the accumulator has been read: the MMA warp may
+          // reuse it
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive_cluster(tempty_leader[acc]);
+        } else if (kPipeTmem) {
+          __syncwarp();
+          ptx::tmem_ld32(tb + (ch + 1) * 32, rbuf[(ch + 1) & 1]);
+        }
         // staging box: the tile's 64-column box, or (Gram) the warp's one box
         const int sbx = kSmallStg ? colhalf : (c0 >> 6);
         const uint32_t rowa = stg_a + sbx * ((kBM / 2) * 128) + row_local * 128;
@@ -566,11 +587,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             ptx::tma_store_3d(&C.tmAux, fslot + my_rows, tl.J * kBN + c0, tl.I * kBM + rowoff + q * kEpiRows,
                               tl.split);
             ptx::bulk_commit();
-          }
-          if (ch == 3) {
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive_cluster(tempty_leader[acc]);
           }
           continue;
         }
@@ -682,12 +698,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const float o = (j & 1) ? word_hi(ow[j >> 1]) : word_lo(ow[j >> 1]);
             if (rt < C.m && ct + j < C.n) pc[static_cast<long long>(j) * C.m] = fmaf(-P.lr, o, pv[j]);
           }
-        }
-        if (ch == 3) {
-          // accumulator drained: the MMA warp may reuse it
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive_cluster(tempty_leader[acc]);
         }
         if (ch & 1) {
           // this warp's rows of box 2*colhalf + ch/2 are written: store them
