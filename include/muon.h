@@ -180,6 +180,17 @@ muon_status_t ns5_workspace_layout(int batch, int64_t rows, int64_t cols, muon_w
  * Returns 0 on success, -1 for an unknown key. */
 int muon_set_debug(const char* key, long long value);
 
+/* Device-side checks of the debug build (libmuon_debug.so, compiled with
+ * MUON_DEBUG): its kernels check the ranges of their raw-pointer accesses
+ * and the alignment of their TMA coordinates; a failed check skips the
+ * access (a skipped copy makes the kernel's bounded wait expire) and is
+ * counted instead of trapping.  Synchronises the device, writes the number
+ * of failed checks since the last call to *failures and clears the
+ * counters.  Returns 0 in the debug build, -1 in the release build (which
+ * has no checks; *failures = 0) or for a null argument, -2 if reading the
+ * counters failed. */
+int muon_debug_check_failures(long long* failures);
+
 /* Waits for the events recorded since the last call (see
  * "record_kernel_events") and returns, per kernel kind, the summed
  * milliseconds and the launch count: kind 0 momentum_cast, 1 normalise,

@@ -17,6 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libmuon.so")
+DEBUG_LIB = os.path.join(LIBDIR, "libmuon_debug.so")  # device-side checks (MUON_DEBUG)
 SOURCES = ["muon_capi.cu", "elementwise.cu", "ns_gemm.cu", "fp8.cu", "noalloc.cu", "partition.cu", "adam.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -33,8 +34,8 @@ def flags():
                    "-I", os.path.join(ROOT, "include"), "-I", CSRC]
 
 
-def _compile(src, extra):
-    out = os.path.join(OBJ, os.path.splitext(src)[0] + ".o")
+def _compile(src, extra, obj_dir):
+    out = os.path.join(obj_dir, os.path.splitext(src)[0] + ".o")
     cmd = [nvcc(), "-c", os.path.join(CSRC, src), "-o", out] + flags() + extra
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -42,23 +43,35 @@ def _compile(src, extra):
     return out, r.stderr
 
 
-def build(verbose=False, extra=()):
-    os.makedirs(OBJ, exist_ok=True)
-    os.makedirs(LIBDIR, exist_ok=True)
-    extra = list(extra)
-    with concurrent.futures.ThreadPoolExecutor(len(SOURCES)) as ex:
-        results = list(ex.map(lambda s: _compile(s, extra), SOURCES))
-    objs = [o for o, _ in results]
-    if verbose:
-        for _, err in results:
-            if err.strip():
-                print(err, file=sys.stderr)
-    tmp = LIB + ".tmp"
+def _link(objs, lib):
+    tmp = lib + ".tmp"
     cmd = [nvcc(), "-shared", "-o", tmp] + objs + ARCH + ["-lcudart_static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
+
+
+def build(verbose=False, extra=(), debug=True):
+    """Builds libmuon.so and, with debug=True, libmuon_debug.so (the same
+    sources with -DMUON_DEBUG), every translation unit in parallel."""
+    os.makedirs(LIBDIR, exist_ok=True)
+    extra = list(extra)
+    variants = [(OBJ, extra, LIB)]
+    if debug:
+        variants.append((OBJ + "_debug", extra + ["-DMUON_DEBUG"], DEBUG_LIB))
+    jobs = []
+    for obj_dir, ex, _ in variants:
+        os.makedirs(obj_dir, exist_ok=True)
+        jobs += [(src, ex, obj_dir) for src in SOURCES]
+    with concurrent.futures.ThreadPoolExecutor(len(jobs)) as pool:
+        results = list(pool.map(lambda j: _compile(*j), jobs))
+    if verbose:
+        for _, err in results:
+            if err.strip():
+                print(err, file=sys.stderr)
+    for k, (_, _, lib) in enumerate(variants):
+        _link([o for o, _ in results[k * len(SOURCES):(k + 1) * len(SOURCES)]], lib)
     return LIB
 
 

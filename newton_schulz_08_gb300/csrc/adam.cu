@@ -32,6 +32,7 @@
 #include <vector>
 
 #include "../../include/muon.h"
+#include "check.cuh"
 
 namespace muon {
 
@@ -85,6 +86,8 @@ __global__ void __launch_bounds__(kAdamThreads) adam_kernel(const __grid_constan
   const AdamTensor& T = P.t[lo];
   const long long e0 = static_cast<long long>(blockIdx.x - P.block_begin[lo]) * kAdamBlockElems;
   const long long e1 = min(T.numel, e0 + kAdamBlockElems);
+  // debug build: the block starts inside its tensor
+  if (!MUON_CHECK(e0 >= 0 && e0 < T.numel)) return;
   // whole vectors of this block; the tensor's last partial vector is done
   // element by element
   const long long nvec = (e1 - e0) / kAdamVec;
@@ -144,6 +147,10 @@ bool overlap(const Span& a, const Span& b) { return a.lo < b.hi && b.lo < a.hi; 
 
 }  // namespace
 
+}  // namespace muon
+
+namespace muon {
+MUON_CHECK_READER(check_failures_adam)
 }  // namespace muon
 
 extern "C" muon_status_t adam_step(const adam_tensor_desc* tensors, int n_tensors, float lr, float beta1,

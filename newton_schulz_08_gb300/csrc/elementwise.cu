@@ -20,6 +20,7 @@
 // apply: after the last step, O = X in the stored orientation written
 //   (Newton-Schulz alone), or p <- p - lr * O for a Muon step with no
 //   iteration (otherwise the last update applies it).
+#include "check.cuh"
 #include "plan.h"
 
 namespace muon {
@@ -99,6 +100,8 @@ __global__ void __launch_bounds__(kEwThreads, 4) momentum_cast_kernel(const __gr
   const int b = blockIdx.x - P.block_begin[lo];
   const int R = M.R, C = M.C;
   float ss = 0.0f;
+  // debug build: the block lies inside its matrix's partial sums
+  if (!MUON_CHECK(b >= 0 && b < M.nparts && M.rows_per_block > 0)) return;
 
   if (b == 0 && threadIdx.x == 0) {
     MatInfo mi;
@@ -147,7 +150,7 @@ __global__ void __launch_bounds__(kEwThreads, 4) momentum_cast_kernel(const __gr
             ss = fmaf(x0, x0, ss);
             ss = fmaf(x1, x1, ss);
           }
-          *reinterpret_cast<uint4*>(M.x + iv[h]) = w[h];
+          if (MUON_CHECK(iv[h] + 8 <= static_cast<long long>(R) * M.ldx)) *reinterpret_cast<uint4*>(M.x + iv[h]) = w[h];
         }
       }
     } else if (vec) {
@@ -215,7 +218,8 @@ __global__ void __launch_bounds__(kEwThreads, 4) momentum_cast_kernel(const __gr
             ss = fmaf(x1, x1, ss);
           }
           const long long r = iv[h] / C, c = iv[h] % C;
-          *reinterpret_cast<uint4*>(M.x + r * M.ldx + c) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+          if (MUON_CHECK(iv[h] + 8 <= static_cast<long long>(R) * C && c + 8 <= M.ldx))
+            *reinterpret_cast<uint4*>(M.x + r * M.ldx + c) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
         }
       }
     } else {
@@ -251,7 +255,7 @@ __global__ void __launch_bounds__(kEwThreads, 4) momentum_cast_kernel(const __gr
       const int c = c0 + cc;
       if (c < cb1) {
         __nv_bfloat16* xd = M.x + static_cast<long long>(c) * M.ldx + r0 + rb;
-        if (r0 + rb + 16 <= R) {
+        if (r0 + rb + 16 <= R && MUON_CHECK(r0 + rb + 16 <= M.ldx && c < C)) {
           uint32_t w[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
@@ -373,6 +377,8 @@ __global__ void __launch_bounds__(kEwThreads, 5) normalise_kernel(const __grid_c
   const int local = blockIdx.x - K.block_begin;
   const int idx = local / K.blocks_per_mat;
   const int b = local - idx * K.blocks_per_mat;
+  // debug build: the block's rows lie inside its class and matrix
+  if (!MUON_CHECK(idx < K.count && b * K.rows_per_block < K.m)) return;
   const MatInfo mi = P.table[K.mat_begin + idx];
 
   __nv_bfloat16* X = K.x + static_cast<long long>(idx) * K.m * K.ldx;
@@ -468,6 +474,10 @@ __global__ void __launch_bounds__(kEwThreads) apply_kernel(const __grid_constant
   const MatInfo mi = P.table[K.mat_begin + idx];
   const __nv_bfloat16* X = K.x + static_cast<long long>(idx) * K.m * K.ldx;
   const int m = K.m, n = K.n;
+  // debug build: the tile lies inside its matrix, whose recorded shape is
+  // the class's
+  if (!MUON_CHECK(idx < K.count && r0 < m && c0 < n && (mi.tall ? mi.C == m && mi.R == n : mi.R == m && mi.C == n)))
+    return;
   const int tid = threadIdx.x;
   const bool param = P.final_mode == kFinalParam;
   if (!mi.tall) {
@@ -621,5 +631,7 @@ cudaError_t launch_normalise(const NormParams& P, int blocks, cudaStream_t strea
   void* args[] = {const_cast<NormParams*>(&P)};
   return launch_pdl(reinterpret_cast<const void*>(&normalise_kernel), blocks, args, stream);
 }
+
+MUON_CHECK_READER(check_failures_elementwise)
 
 }  // namespace muon

@@ -21,6 +21,7 @@
 // rounds the exact quotient: bf16(x / s) for a bf16 x and a float s.
 #include <cuda_fp8.h>
 
+#include "check.cuh"
 #include "plan.h"
 
 namespace muon {
@@ -211,7 +212,8 @@ __global__ void __launch_bounds__(kThreads) fp8_transpose_kernel(const __grid_co
       if (r < J.rows && c < J.cols) {
         a = quantise8<true>(v[p][0], J.scale, J.inv_scale);
         b = quantise8<true>(v[p][1], J.scale, J.inv_scale);
-        *reinterpret_cast<uint4*>(J.dst + static_cast<long long>(r) * J.cols + c) = make_uint4(a.x, a.y, b.x, b.y);
+        if (MUON_CHECK(c + 16 <= J.cols && (c & 15) == 0))
+          *reinterpret_cast<uint4*>(J.dst + static_cast<long long>(r) * J.cols + c) = make_uint4(a.x, a.y, b.x, b.y);
       }
       *reinterpret_cast<uint4*>(&tile[slot(rl, cl >> 2)]) = make_uint4(a.x, a.y, b.x, b.y);
     }
@@ -252,7 +254,7 @@ __global__ void __launch_bounds__(kThreads) fp8_transpose_kernel(const __grid_co
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int c = c0 + 4 * wc + i;
-      if (c < J.cols)
+      if (c < J.cols && MUON_CHECK(rr + 16 <= J.rows && (rr & 15) == 0))
         *reinterpret_cast<uint4*>(J.dst_t + static_cast<long long>(c) * J.rows + rr) =
             make_uint4(o[i][0], o[i][1], o[i][2], o[i][3]);
     }
@@ -269,6 +271,7 @@ __global__ void __launch_bounds__(kThreads) fp8_reduce_kernel(const __grid_const
   grid_dep();
   const long long i = (static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x) * 4;
   if (i >= P.n) return;
+  if (!MUON_CHECK(i + 4 <= P.n)) return;
   float4 acc = *reinterpret_cast<const float4*>(P.part + i);
   for (int s = 1; s < P.splits; ++s) {
     const float4 v = *reinterpret_cast<const float4*>(P.part + static_cast<long long>(s) * P.n + i);
@@ -289,5 +292,7 @@ cudaError_t launch_fp8_reduce(const Fp8ReduceParams& P, int blocks, cudaStream_t
   void* args[] = {const_cast<Fp8ReduceParams*>(&P)};
   return launch_pdl(reinterpret_cast<const void*>(&fp8_reduce_kernel), blocks, args, stream);
 }
+
+MUON_CHECK_READER(check_failures_fp8)
 
 }  // namespace muon

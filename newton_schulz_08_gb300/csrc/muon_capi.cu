@@ -29,6 +29,7 @@
 #include <vector>
 
 #include "../../include/muon.h"
+#include "check.cuh"
 #include "plan.h"
 #include "ptx.cuh"
 
@@ -1051,6 +1052,27 @@ int muon_set_debug(const char* key, long long value) {
     return 0;
   }
   return -1;
+}
+
+int muon_debug_check_failures(long long* failures) {
+  if (!failures) return -1;
+  *failures = 0;
+#ifdef MUON_DEBUG
+  long long total = 0;
+  for (cudaError_t (*f)(int*) : {&check_failures_elementwise, &check_failures_gemm, &check_failures_fp8,
+                                 &check_failures_adam}) {
+    int v = 0;
+    if (f(&v) != cudaSuccess) {
+      cudaGetLastError();
+      return -2;
+    }
+    total += v;
+  }
+  *failures = total;
+  return 0;
+#else
+  return -1;
+#endif
 }
 
 void muon_plan_cache_clear(void) {

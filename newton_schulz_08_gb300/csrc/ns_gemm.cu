@@ -59,6 +59,7 @@
 // drain, frees TMEM and returns.
 #include <mutex>
 
+#include "check.cuh"
 #include "plan.h"
 #include "ptx.cuh"
 
@@ -246,6 +247,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           if (prof) prof[kWpProducerEmpty] += clock64() - w0;
+          // debug build: every copy's inner coordinate is a whole number of
+          // 16-byte units and non-negative (an unaligned one faults)
+          if (!MUON_CHECK(kb * kKB >= 0 && (kb * kKB) % 8 == 0 && (tl.I * kBM + half) % 8 == 0 &&
+                          (tl.J * kBN + half) % 8 == 0)) {
+            raise_timeout(P, abort);
+            ok = false;
+            break;
+          }
           const uint32_t fb = ptx::map_to_rank(ptx::smem_addr(&full[stage]), 0);
           const uint32_t sa = ptx::smem_addr(smem + stage * kStageBytes);
           const uint32_t sb = sa + kStageA;
@@ -396,6 +405,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     };
     auto store_box = [&](const GemmClass& C, const Tile& tl, int bx) {
       const int sbx = kSmallStg ? colhalf : bx;
+      if (!MUON_CHECK(tl.J * kBN + 64 * bx >= 0 && (tl.J * kBN + 64 * bx) % 8 == 0 && tl.I >= 0)) return;
       ptx::tma_store_3d(&C.tmOut, stg_a + sbx * (kBM / 2) * 128 + my_rows, tl.J * kBN + 64 * bx,
                         tl.I * kBM + rowoff + q * kEpiRows, tl.idx);
       ptx::bulk_commit();
@@ -476,6 +486,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int x, y;
       p_xy(tn, P.table[Cn.mat_begin + tn.idx].tall, ch, &x, &y);
       const uint32_t bar = ptx::smem_addr(&pfull[(warp - 2) * 2 + sl]);
+      // debug build: fp32 boxes start on 4-element columns (16 bytes); the
+      // block is then skipped and its wait expires (bounded)
+      if (!MUON_CHECK(x >= 0 && y >= 0 && x % 4 == 0)) return;
       ptx::mbar_arrive_expect_tx(bar, kPSlot);
       ptx::tma_load_2d(pslot0 + sl * kPSlot, p_map(Cn, tn), bar, x, y);
     };
@@ -500,6 +513,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const MatInfo& mi = P.table[C.mat_begin + tl.idx];
         pm = static_cast<float*>(mi.out);
         ptall = mi.tall != 0;
+        // debug build: the parameter recorded for this matrix has the class's shape
+        if (!MUON_CHECK(ptall ? (mi.C == C.m && mi.R == C.n) : (mi.R == C.m && mi.C == C.n))) pm = nullptr;
       }
       if (!kNoAux) {
         if (!ptx::mbar_wait(ptx::smem_addr(my_aux), aux_phase, budget, abort)) {
@@ -540,7 +555,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         float* pc = nullptr;
         const int rt = tl.I * kBM + rowoff + row_local;
         const int ct = tl.J * kBN + c0;
-        if (MODE == kUpdate && fuse && ptall && !bulkp) {
+        if (MODE == kUpdate && fuse && ptall && !bulkp && pm) {
           pc = pm + static_cast<long long>(ct) * C.m + rt;
 #pragma unroll
           for (int j = 0; j < 32; ++j)
@@ -688,11 +703,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (lane == 0 && !*abort) {
             int x, y;
             p_xy(tl, ptall, ch, &x, &y);
-            ptx::tma_store_2d(p_map(C, tl), slot, x, y);
+            if (MUON_CHECK(x >= 0 && y >= 0 && x % 4 == 0)) ptx::tma_store_2d(p_map(C, tl), slot, x, y);
             ptx::bulk_commit();
           }
         }
-        if (MODE == kUpdate && fuse && ptall && !bulkp) {
+        if (MODE == kUpdate && fuse && ptall && !bulkp && pm) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const float o = (j & 1) ? word_hi(ow[j >> 1]) : word_lo(ow[j >> 1]);
@@ -703,7 +718,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           // this warp's rows of box 2*colhalf + ch/2 are written: store them
           // (or apply them to p)
           if (MODE == kUpdate && fuse) {
-            if (!ptall && !bulkp) apply_box(C, tl, pm, 2 * colhalf + (ch >> 1));
+            if (!ptall && !bulkp && pm) apply_box(C, tl, pm, 2 * colhalf + (ch >> 1));
           } else {
             ptx::fence_async_smem();
             __syncwarp();
@@ -899,5 +914,7 @@ cudaError_t launch_ns_gemm(int mode, int variant, const GemmParams& P, int pairs
   void* args[] = {const_cast<GemmParams*>(&P)};
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
+
+MUON_CHECK_READER(check_failures_gemm)
 
 }  // namespace muon

@@ -14,6 +14,8 @@ import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "lib", "libmuon.so")
+#: the same library with device-side checks (tests and debugging)
+DEBUG_LIB_PATH = os.path.join(_PKG, "lib", "libmuon_debug.so")
 
 MUON_OK = 0
 MUON_WARN_NONFINITE = 1
@@ -34,7 +36,7 @@ EXPORTS = ["muon_workspace_size", "muon_step", "ns5_workspace_size", "ns5", "ns5
            "ns5_bank_workspace_size", "muon_device_status", "muon_status_str",
            "ns5_workspace_layout", "muon_set_debug", "muon_kernel_times", "ns5_noalloc",
            "muon_partition", "adam_step", "fp8_mm", "muon_plan_cache_clear",
-           "fp8_mm_backward", "fp8_mm_backward_workspace_size"]
+           "fp8_mm_backward", "fp8_mm_backward_workspace_size", "muon_debug_check_failures"]
 
 #: bytes of the static device scratch ns5_noalloc uses (MUON_NOALLOC_SCRATCH_BYTES)
 NOALLOC_SCRATCH_BYTES = 64 << 20
@@ -74,12 +76,18 @@ _lib = None
 def lib():
     """The loaded library (raises if it has not been built)."""
     global _lib
-    if _lib is not None:
-        return _lib
-    if not os.path.exists(LIB_PATH):
-        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+    if _lib is None:
+        _lib = load(LIB_PATH)
+    return _lib
+
+
+def load(path):
+    """A ctypes handle on the library at `path` with every entry point's
+    signature declared (the release library, or the debug build)."""
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with "
                            "`python -m newton_schulz_08_gb300.build` (or __graft_entry__.build())")
-    L = ctypes.CDLL(LIB_PATH)
+    L = ctypes.CDLL(path)
     c_int, c_i64, c_sz, c_vp, c_f = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
     P = ctypes.POINTER
     L.muon_workspace_size.argtypes = [P(muon_mat_desc), c_int]
@@ -120,7 +128,8 @@ def lib():
     L.fp8_mm_backward.restype = c_int
     L.muon_plan_cache_clear.argtypes = []
     L.muon_plan_cache_clear.restype = None
-    _lib = L
+    L.muon_debug_check_failures.argtypes = [P(ctypes.c_longlong)]
+    L.muon_debug_check_failures.restype = c_int
     return L
 
 

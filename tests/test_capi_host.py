@@ -297,3 +297,13 @@ def test_fp8_backward_argument_errors(L, case, code):
     st = L.fp8_mm_backward(vp(a["g"]), vp(a["x"]), vp(a["w"]), a["xs"], a["ws_"], a["gs"], vp(a["gx"]), vp(a["gw"]),
                            vp(a["gq"]), a["M"], a["N"], a["K"], vp(a["wsp"]), a["wsb"], None)
     assert st == code
+
+
+def test_debug_build_exports_and_release_reports_no_checks(L):
+    import ctypes
+    D = muon.load(muon.DEBUG_LIB_PATH)
+    for n in declared_functions():
+        assert hasattr(D, n), n
+    n = ctypes.c_longlong(-5)
+    assert L.muon_debug_check_failures(n) == -1 and n.value == 0  # release: no checks
+    assert L.muon_debug_check_failures(None) == -1
