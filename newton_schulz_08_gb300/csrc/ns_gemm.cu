@@ -586,12 +586,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           // slot as one fp32 box, stored to the slice's plane of the
           // partial-sum array once the previous chunk's box has been read
           // (two slots per warp, used in turn: a slot is rewritten once the
-          // store two chunks back has read it)
+          // store two chunks back -- possibly of the previous tile -- has
+          // read it)
           const uint32_t fslot = stg_a + (2 * colhalf + (ch & 1)) * ((kBM / 2) * 128);
-          if (ch > 1) {
-            if (lane == 0) ptx::bulk_wait_read1();
-            __syncwarp();
-          }
+          if (lane == 0) ptx::bulk_wait_read1();
+          __syncwarp();
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             ptx::sts128(fslot + row_local * 128 + ((j ^ (row_local & 7)) << 4), r[4 * j], r[4 * j + 1], r[4 * j + 2],
@@ -608,6 +607,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (kSmallStg && ch == 2) {
           // the warp's box still holds its first half until the store has read it
           if (lane == 0) ptx::bulk_wait_read0();
+          __syncwarp();
+        }
+        if (MODE == kFp8 && (ch & 1) == 0) {
+          // the FP8 product stages no input, so a tile's stores need not be
+          // read before the next tile starts: a box is rewritten once its
+          // store from the previous tile has read it (one younger store may
+          // still be pending)
+          if (lane == 0) ptx::bulk_wait_read1();
           __syncwarp();
         }
         const int j0 = (c0 & 63) >> 3;
@@ -759,7 +766,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         __syncwarp();
       }
       if (lane == 0) {
-        ptx::bulk_wait_read0();  // this warp's rows are free again
+        if (MODE != kFp8) ptx::bulk_wait_read0();  // this warp's rows are free again
         if (!kNoAux && t + npairs < P.total_tiles) {
           ptx::fence_async_smem();
           load_aux(t + npairs);
