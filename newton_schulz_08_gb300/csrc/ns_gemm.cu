@@ -325,32 +325,49 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (prof) prof[kWpMmaTempty] += clock64() - w1;
         ptx::tc_fence_after();
         const uint32_t d = tmem_base + acc * kBN;
-        for (int kb = kb0; kb < kb1; ++kb) {
-          const long long w2 = prof ? clock64() : 0;
-          if (!ptx::mbar_wait(ptx::smem_addr(&full[stage]), phase, budget, abort)) {
-            raise_timeout(P, abort);
-            ok = false;
-            break;
-          }
-          if (prof) prof[kWpMmaFull] += clock64() - w2;
-          ptx::tc_fence_after();
-          const uint32_t sa = ptx::smem_addr(smem + stage * kStageBytes);
+        // One K block: its stage's operands are waited for, then its four
+        // MMAs issue back to back.  Everything they take is formed before
+        // the wait.  A descriptor's low 14 bits are the operand address / 16,
+        // so the k-th MMA's descriptor is the first one plus k steps: 32
+        // bytes (16 K elements of a 128-byte row) K-major, 2048 bytes (16 rows
+        // of 128 bytes) MN-major.  Shared addresses stay below 2^18, so the
+        // sum never carries out of the field.
+        auto kblock = [&](int st, uint32_t ph, int kb) -> bool {
+          const uint32_t sa = ptx::smem_addr(smem + st * kStageBytes);
           const uint32_t sb = sa + kStageA;
           const int jb = kb * kBK / kBN;
           const bool a_mn = (MODE == kPoly || MODE == kUpdate) && SYM && jb < tl.I;
           const bool b_mn = MODE == kUpdate || (MODE == kPoly && SYM && jb < tl.J);
-          const uint32_t idesc = a_mn ? (b_mn ? idesc_mm : idesc_mk) : (b_mn ? idesc_km : idesc_kk);
+          const uint32_t idesc =
+              MODE == kFp8 ? P.idesc_f8 : (a_mn ? (b_mn ? idesc_mm : idesc_mk) : (b_mn ? idesc_km : idesc_kk));
+          const uint64_t a0 = a_mn ? ptx::sdesc_sw128(sa, 64 * kBK * 2, 1024) : ptx::sdesc_sw128(sa, 16, 1024);
+          const uint64_t b0 = b_mn ? ptx::sdesc_sw128(sb, 64 * kBK * 2, 1024) : ptx::sdesc_sw128(sb, 16, 1024);
+          const uint64_t astep = a_mn ? 2048 / 16 : 32 / 16;
+          const uint64_t bstep = b_mn ? 2048 / 16 : 32 / 16;
+          const uint32_t acc0 = kb != kb0 ? 1u : 0u;
+          const long long w2 = prof ? clock64() : 0;
+          if (!ptx::mbar_wait(ptx::smem_addr(&full[st]), ph, budget, abort)) return false;
+          if (prof) prof[kWpMmaFull] += clock64() - w2;
+          ptx::tc_fence_after();
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
-            const uint64_t adesc = a_mn ? ptx::sdesc_sw128(sa + k * 2048, 64 * kBK * 2, 1024)
-                                        : ptx::sdesc_sw128(sa + k * 32, 16, 1024);
-            const uint64_t bdesc = b_mn ? ptx::sdesc_sw128(sb + k * 2048, 64 * kBK * 2, 1024)
-                                        : ptx::sdesc_sw128(sb + k * 32, 16, 1024);
-            const uint32_t accum = (kb != kb0 || k != 0) ? 1u : 0u;
             if (MODE == kFp8)
-              ptx::mma_f8_pair(d, adesc, bdesc, P.idesc_f8, accum);
+              ptx::mma_f8_pair(d, a0 + k * astep, b0 + k * bstep, idesc, k == 0 ? acc0 : 1u);
             else
-              ptx::mma_bf16_pair(d, adesc, bdesc, idesc, accum);
+              ptx::mma_bf16_pair(d, a0 + k * astep, b0 + k * bstep, idesc, k == 0 ? acc0 : 1u);
+          }
+          return true;
+        };
+        // Each stage is released as soon as its MMAs are issued (the commit
+        // arrives once they have completed).  Releasing stages in pairs after
+        // eight MMAs issues the MMAs with fewer pauses, but it holds every
+        // first stage of a pair for four more MMAs, and the operand ring then
+        // runs dry more often: measured slower on every phase.
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!kblock(stage, phase, kb)) {
+            raise_timeout(P, abort);
+            ok = false;
+            break;
           }
           ptx::mma_commit_pair_mc(ptx::smem_addr(&empty[stage]), 0x3);
           if (++stage == kSt) {
