@@ -30,6 +30,7 @@ namespace {
 constexpr int kEwThreads = 256;
 constexpr int kNormBatch = 4;  // normalise: 8-element vectors per thread in flight
 constexpr int kCastBatch = 8;  // cast-only momentum pass: 8-element vectors per thread in flight
+constexpr int kMomBatch = 2;   // momentum pass with bf16 G: 8-element vectors per thread in flight
 
 // Programmatic dependent launch: wait for the previous grid's results, then
 // let the next grid be scheduled.
@@ -151,6 +152,55 @@ __global__ void __launch_bounds__(kEwThreads, 4) momentum_cast_kernel(const __gr
             ss = fmaf(x1, x1, ss);
           }
           if (MUON_CHECK(iv[h] + 8 <= static_cast<long long>(R) * M.ldx)) *reinterpret_cast<uint4*>(M.x + iv[h]) = w[h];
+        }
+      }
+    } else if (vec && M.buf && !M.g_f32) {
+      // momentum and cast, bf16 G: rows [r0, r1) are contiguous in g, buf
+      // and X (a wide matrix's X pitch is C when C is a multiple of 8).
+      // kMomBatch 8-element vectors per thread, all their loads (16 bytes
+      // of g, 32 of buf) issued before any store: 48 bytes per vector
+      const long long base = static_cast<long long>(r0) * C;
+      const int nvec = (r1 - r0) * (C >> 3);
+      const uint4* gv = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(M.g) + base);
+      float4* bv4 = reinterpret_cast<float4*>(M.buf + base);
+      uint4* xv = reinterpret_cast<uint4*>(M.x + base);
+      // debug build: the block's rows lie inside the matrix and X's pitch is C
+      if (!MUON_CHECK(M.ldx == C && r1 <= R)) return;
+      for (int v0 = threadIdx.x; v0 < nvec; v0 += kMomBatch * kEwThreads) {
+        uint4 gw[kMomBatch];
+        float4 b0[kMomBatch], b1[kMomBatch];
+#pragma unroll
+        for (int h = 0; h < kMomBatch; ++h) {
+          const int v = v0 + h * kEwThreads;
+          if (v < nvec) {
+            gw[h] = __ldg(gv + v);
+            b0[h] = bv4[2 * v];
+            b1[h] = bv4[2 * v + 1];
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < kMomBatch; ++h) {
+          const int v = v0 + h * kEwThreads;
+          if (v >= nvec) continue;
+          const uint32_t ws[4] = {gw[h].x, gw[h].y, gw[h].z, gw[h].w};
+          float b[8] = {b0[h].x, b0[h].y, b0[h].z, b0[h].w, b1[h].x, b1[h].y, b1[h].z, b1[h].w};
+          uint32_t packed[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float g0 = __uint_as_float(ws[k] << 16), g1 = __uint_as_float(ws[k] & 0xFFFF0000u);
+            b[2 * k] = fmaf(P.mu, b[2 * k], g0);
+            b[2 * k + 1] = fmaf(P.mu, b[2 * k + 1], g1);
+            const float u0 = P.nesterov ? fmaf(P.mu, b[2 * k], g0) : b[2 * k];
+            const float u1 = P.nesterov ? fmaf(P.mu, b[2 * k + 1], g1) : b[2 * k + 1];
+            const __nv_bfloat162 hh = __floats2bfloat162_rn(u0, u1);
+            packed[k] = *reinterpret_cast<const uint32_t*>(&hh);
+            const float x0 = __low2float(hh), x1 = __high2float(hh);
+            ss = fmaf(x0, x0, ss);
+            ss = fmaf(x1, x1, ss);
+          }
+          bv4[2 * v] = make_float4(b[0], b[1], b[2], b[3]);
+          bv4[2 * v + 1] = make_float4(b[4], b[5], b[6], b[7]);
+          xv[v] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
         }
       }
     } else if (vec) {
