@@ -440,20 +440,21 @@ __global__ void __launch_bounds__(kEwThreads, 5) normalise_kernel(const __grid_c
   const long long nvec = vec ? static_cast<long long>(r1 - r0) * cv : 0;
   // a batch: kNormBatch vectors of 8 per thread, all loads issued before any
   // store; the first batch is loaded before the norm is known, so that the
-  // reduction of the partials below overlaps its latency
+  // reduction of the partials below overlaps its latency.  With n a multiple
+  // of 8 the row pitch is n, so the block's rows [r0, r1) are one contiguous
+  // run of nvec vectors.
+  (void)cv;
+  // debug build: the vector path's rows are contiguous
+  if (vec && !MUON_CHECK(K.ldx == n)) return;
+  uint4* const xv = reinterpret_cast<uint4*>(X + static_cast<long long>(r0) * n);
   uint4 w[kNormBatch];
-  uint4* ptr[kNormBatch];
   bool have[kNormBatch];
   auto load_batch = [&](long long v0) {
 #pragma unroll
     for (int h = 0; h < kNormBatch; ++h) {
       const long long v = v0 + h * kEwThreads;
       have[h] = v < nvec;
-      const long long vv = have[h] ? v : 0;
-      const int r = r0 + static_cast<int>(vv / cv);
-      const int cc = static_cast<int>(vv % cv) * 8;
-      ptr[h] = reinterpret_cast<uint4*>(X + static_cast<long long>(r) * K.ldx + cc);
-      if (have[h]) w[h] = *ptr[h];
+      if (have[h]) w[h] = xv[v];
     }
   };
   if (vec) load_batch(threadIdx.x);
@@ -489,7 +490,7 @@ __global__ void __launch_bounds__(kEwThreads, 5) normalise_kernel(const __grid_c
           const __nv_bfloat162 hh = __floats2bfloat162_rn(lo, hi);
           ws[k] = *reinterpret_cast<const uint32_t*>(&hh);
         }
-        *ptr[h] = make_uint4(ws[0], ws[1], ws[2], ws[3]);
+        xv[v0 + h * kEwThreads] = make_uint4(ws[0], ws[1], ws[2], ws[3]);
       }
     }
   } else {
