@@ -176,6 +176,7 @@ constexpr int kMaxPMaps = 190;
 struct GemmParamsP : GemmParams {
   CUtensorMap pmap[kMaxPMaps];
 };
+static_assert(sizeof(GemmParamsP) <= 32764, "kernel parameters are limited to 32764 bytes");
 template <int APPLY>
 struct GemmParamsOf {
   using type = GemmParams;

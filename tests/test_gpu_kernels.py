@@ -360,6 +360,32 @@ def test_parameter_update_is_one_fma_per_entry(shape):
     assert same.all(), (int((~same).sum()), got.size)
 
 
+def test_last_update_of_a_bank_beyond_the_streamed_maps():
+    """A bank of more matrices than one launch carries parameter maps for
+    (230, against 190): the last update takes the register path over three
+    shape classes.  With momentum 0 the step's O is ns5_bank's O of the same
+    gradients bit for bit, and every parameter must equal fl32(p - lr O)."""
+    shapes = [(64, 128)] * 100 + [(128, 64)] * 100 + [(96, 200)] * 30
+    lr = np.float32(0.02)
+    dev = torch.device("cuda")
+    ps = [inputs.param(s, 500 + i) for i, s in enumerate(shapes)]
+    gs = [oracle.round_to_bf16(inputs.grad(s, 500 + i)).astype(np.float32) for i, s in enumerate(shapes)]
+    P = [torch.from_numpy(p).to(dev) for p in ps]
+    G = [torch.from_numpy(g).to(dev).to(torch.bfloat16) for g in gs]
+    B = [torch.zeros_like(x) for x in P]
+    ws = muon.muon_step(P, G, B, lr=float(lr), momentum=0.0, nesterov=True, ns_steps=5)
+    O = muon.ns5_bank([g.float() for g in G], 5)
+    torch.cuda.synchronize()
+    check_status(ws)
+    bad = 0
+    for i in range(len(shapes)):
+        o = O[i].float().cpu().numpy().astype(np.float64)
+        want = (ps[i].astype(np.float64) - np.float64(lr) * o).astype(np.float32)
+        got = P[i].cpu().numpy()
+        bad += int((got.view(np.uint32) != want.view(np.uint32)).sum())
+    assert bad == 0, bad
+
+
 def test_zero_lr_and_zero_momentum():
     """lr = 0 leaves the parameters bit for bit; momentum 0 makes the buffer
     the gradient (fp32 value of the bf16 gradient)."""
