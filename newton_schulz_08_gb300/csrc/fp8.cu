@@ -97,17 +97,8 @@ __device__ __forceinline__ uint32_t to_e5m2(float v) {
 __device__ __forceinline__ float word_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float word_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// The two bf16 quotients of a pair (lo, hi): when both take the fast path
-// they are rounded by one paired conversion.
-__device__ __forceinline__ float2 div2_to_bf16(float x0, float x1, float s, float inv) {
-  const float q0 = x0 * inv, q1 = x1 * inv;
-  const uint32_t l0 = __float_as_uint(q0) & 0xFFFFu, l1 = __float_as_uint(q1) & 0xFFFFu;
-  if (isfinite(q0) && isfinite(q1) && l0 - 0x7FFDu > 6u && l1 - 0x7FFDu > 6u)
-    return __bfloat1622float2(__floats2bfloat162_rn(q0, q1));
-  return make_float2(div_to_bf16(x0, s, inv), div_to_bf16(x1, s, inv));
-}
-
-// Two codes (a in the low byte): in range, one paired conversion.
+// Two codes (a in the low byte), range-checked: past the finite range the
+// single conversions give NaN or infinity.
 template <bool E5M2>
 __device__ __forceinline__ uint32_t to_fp8x2(float a, float b) {
   if (E5M2) {
@@ -120,16 +111,34 @@ __device__ __forceinline__ uint32_t to_fp8x2(float a, float b) {
   return to_e4m3(a) | (to_e4m3(b) << 8);
 }
 
+// The codes of the pair (x0, x1): code(bf16(x / s)).  Fast path, taken
+// when both quotients are well inside the code's finite range (|q| below
+// 61000 for E5M2, 460 for E4M3: their bf16 roundings then stay below the
+// overflow thresholds 61440 and 464, and the range test also rules out
+// infinities and NaN) and away from a bf16 rounding boundary (div_to_bf16):
+// one paired bf16 rounding and one paired code conversion.  Otherwise
+// each quotient is rounded exactly and range-checked on its own.
+template <bool E5M2>
+__device__ __forceinline__ uint32_t quantise_pair(float x0, float x1, float s, float inv) {
+  constexpr float kLim = E5M2 ? 61000.0f : 460.0f;
+  const float q0 = x0 * inv, q1 = x1 * inv;
+  const uint32_t l0 = __float_as_uint(q0) & 0xFFFFu, l1 = __float_as_uint(q1) & 0xFFFFu;
+  if (fabsf(q0) < kLim && fabsf(q1) < kLim && l0 - 0x7FFDu > 6u && l1 - 0x7FFDu > 6u) {
+    const float2 v = __bfloat1622float2(__floats2bfloat162_rn(q0, q1));
+    return static_cast<uint32_t>(
+        __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, E5M2 ? __NV_E5M2 : __NV_E4M3));
+  }
+  return to_fp8x2<E5M2>(div_to_bf16(x0, s, inv), div_to_bf16(x1, s, inv));
+}
+
 // Four bf16 pairs (one 16-byte vector) to 8 one-byte codes (two words).
 template <bool E5M2>
 __device__ __forceinline__ uint2 quantise8(uint4 w, float s, float inv) {
   const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
   uint32_t out[2] = {0u, 0u};
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float2 q = div2_to_bf16(word_lo(ws[k]), word_hi(ws[k]), s, inv);
-    out[k >> 1] |= to_fp8x2<E5M2>(q.x, q.y) << (16 * (k & 1));
-  }
+  for (int k = 0; k < 4; ++k)
+    out[k >> 1] |= quantise_pair<E5M2>(word_lo(ws[k]), word_hi(ws[k]), s, inv) << (16 * (k & 1));
   return make_uint2(out[0], out[1]);
 }
 
