@@ -30,7 +30,14 @@ namespace {
 constexpr int kEwThreads = 256;
 constexpr int kNormBatch = 4;  // normalise: 8-element vectors per thread in flight
 constexpr int kCastBatch = 8;  // cast-only momentum pass: 8-element vectors per thread in flight
-constexpr int kMomBatch = 2;   // momentum pass with bf16 G: 8-element vectors per thread in flight
+constexpr int kMomBatch = 2;
+// Tall momentum pass: the 64 x 64 fp32 shared tile has rows of 66 floats and
+// column c of row r stored at c ^ (8 * ((r / 16) % 4)).  A warp's writes (two
+// rows, four consecutive columns per lane, the upper half-warp's in rotated
+// order) and its reads (column cc of rows rb + 2j, rb a multiple of 16) then
+// fall in 32 different banks.
+constexpr int kTallPitch = 66;
+__device__ __forceinline__ int tall_col(int r, int c) { return c ^ (((r >> 4) & 3) << 3); }   // momentum pass with bf16 G: 8-element vectors per thread in flight
 
 // Programmatic dependent launch: wait for the previous grid's results, then
 // let the next grid be scheduled.
@@ -90,7 +97,7 @@ __device__ __forceinline__ float momentum_u(float g, float* buf, long long i, fl
 __global__ void __launch_bounds__(kEwThreads, 4) momentum_cast_kernel(const __grid_constant__ K1Params P) {
   ptx_grid_dep_wait();
   __shared__ float red[kEwThreads / 32];
-  __shared__ float tile[2][64][65];
+  __shared__ float tile[2][64][kTallPitch];
   // which matrix: largest i with block_begin[i] <= blockIdx.x
   int lo = 0, hi = P.n - 1;
   while (lo < hi) {
@@ -299,7 +306,7 @@ __global__ void __launch_bounds__(kEwThreads, 4) momentum_cast_kernel(const __gr
     const int tid = threadIdx.x;
     const int cl = (tid & 15) * 4;  // tile columns cl .. cl + 3
     const int rq = tid >> 4;        // tile rows rq + 16 k
-    auto write_out = [&](int c0, float (*tl)[65]) {
+    auto write_out = [&](int c0, float (*tl)[kTallPitch]) {
       const int cc = tid >> 2;        // X row c0 + cc
       const int rb = (tid & 3) * 16;  // X columns r0 + rb .. + 15
       const int c = c0 + cc;
@@ -309,13 +316,14 @@ __global__ void __launch_bounds__(kEwThreads, 4) momentum_cast_kernel(const __gr
           uint32_t w[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const __nv_bfloat162 h = __floats2bfloat162_rn(tl[rb + 2 * j][cc], tl[rb + 2 * j + 1][cc]);
+            const __nv_bfloat162 h =
+                __floats2bfloat162_rn(tl[rb + 2 * j][tall_col(rb + 2 * j, cc)], tl[rb + 2 * j + 1][tall_col(rb + 2 * j + 1, cc)]);
             w[j] = *reinterpret_cast<const uint32_t*>(&h);
           }
           reinterpret_cast<uint4*>(xd)[0] = make_uint4(w[0], w[1], w[2], w[3]);
           reinterpret_cast<uint4*>(xd)[1] = make_uint4(w[4], w[5], w[6], w[7]);
         } else {
-          for (int j = 0; j < 16 && r0 + rb + j < R; ++j) xd[j] = __float2bfloat16_rn(tl[rb + j][cc]);
+          for (int j = 0; j < 16 && r0 + rb + j < R; ++j) xd[j] = __float2bfloat16_rn(tl[rb + j][tall_col(rb + j, cc)]);
         }
       }
     };
@@ -380,8 +388,15 @@ __global__ void __launch_bounds__(kEwThreads, 4) momentum_cast_kernel(const __gr
               ss = fmaf(x[j], x[j], ss);
             }
           }
+          // the upper half-warp writes its four columns in rotated order
+          // (bank-conflict-free with the row pitch and column swizzle)
+          const bool rot = (tid & 8) != 0;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) tile[tb][rr][cl + j] = x[j];
+          for (int j = 0; j < 4; ++j) {
+            const int jr = rot ? (j + 1) & 3 : j;
+            const float xv = rot ? x[(j + 1) & 3] : x[j];
+            tile[tb][rr][tall_col(rr, cl + jr)] = xv;
+          }
         }
         // one barrier per tile: the other buffer was last read before the
         // previous tile's barrier
@@ -403,7 +418,7 @@ __global__ void __launch_bounds__(kEwThreads, 4) momentum_cast_kernel(const __gr
               x = bf16_round(momentum_u(load_g(M.g, M.g_f32, i), M.buf, i, P.mu, P.nesterov));
               ss = fmaf(x, x, ss);
             }
-            tile[0][rr][cl + j] = x;
+            tile[0][rr][tall_col(rr, cl + j)] = x;
           }
         }
         __syncthreads();
