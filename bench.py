@@ -399,19 +399,22 @@ def e2e_pipelined(stream, device, n_steps, in_bufs, in_host, step_fn, out_dev, o
     pinned host memory and reads its result back to pinned host memory.  The
     copies run on two copy streams and overlap the compute: step k+1's inputs
     go into the second of two device input buffers while step k runs, and
-    step k's result is snapshotted on the device and read back while step
-    k+1 runs.  in_bufs: two lists of device input tensors; in_host: lists of
-    pinned host tensors (cycled); step_fn(j) runs one step on in_bufs[j];
-    out_dev / out_host: lists of device result tensors and pinned host
-    buffers.  Returns milliseconds per step (CUDA events on `stream`)."""
+    step k's result is snapshotted on the device (into the second of two
+    snapshot buffers, so that the snapshot waits only for the read-back of
+    step k-2) and read back while step k+1 runs.  in_bufs: two lists of
+    device input tensors; in_host: lists of pinned host tensors (cycled);
+    step_fn(j) runs one step on in_bufs[j]; out_dev / out_host: lists of
+    device result tensors and pinned host buffers.  Returns milliseconds per
+    step (CUDA events on `stream`)."""
     import torch
     h2d, d2h = torch.cuda.Stream(device), torch.cuda.Stream(device)
-    snap = [torch.empty_like(t) for t in out_dev]
+    snap = [[torch.empty_like(t) for t in out_dev] for _ in range(2)]
     ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of buffer j landed
     ev_used = [torch.cuda.Event() for _ in range(2)]  # the step reading buffer j finished
-    ev_snap, ev_out = torch.cuda.Event(), torch.cuda.Event()
+    ev_snap = [torch.cuda.Event() for _ in range(2)]  # snapshot j taken
+    ev_out = [torch.cuda.Event() for _ in range(2)]   # snapshot j read back
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for e in ev_used + [ev_out]:
+    for e in ev_used + ev_out:
         e.record(stream)
 
     def upload(k, j):
@@ -430,17 +433,18 @@ def e2e_pipelined(stream, device, n_steps, in_bufs, in_host, step_fn, out_dev, o
         stream.wait_event(ev_in[j])
         step_fn(j)
         ev_used[j].record(stream)
-        stream.wait_event(ev_out)  # the previous snapshot has been read back
+        stream.wait_event(ev_out[j])  # snapshot j (step k-2) has been read back
         with torch.cuda.stream(stream):
-            for dst, src in zip(snap, out_dev):
+            for dst, src in zip(snap[j], out_dev):
                 dst.copy_(src, non_blocking=True)
-        ev_snap.record(stream)
-        d2h.wait_event(ev_snap)
+        ev_snap[j].record(stream)
+        d2h.wait_event(ev_snap[j])
         with torch.cuda.stream(d2h):
-            for dst, src in zip(out_host, snap):
+            for dst, src in zip(out_host, snap[j]):
                 dst.copy_(src, non_blocking=True)
-        ev_out.record(d2h)
-    stream.wait_event(ev_out)
+        ev_out[j].record(d2h)
+    for e in ev_out:
+        stream.wait_event(e)
     e1.record(stream)
     e1.synchronize()
     return e0.elapsed_time(e1) / n_steps
@@ -448,7 +452,8 @@ def e2e_pipelined(stream, device, n_steps, in_bufs, in_host, step_fn, out_dev, o
 
 E2E_NOTE = ("every step uploads its inputs from pinned host memory and reads its result back to pinned host "
             "memory; the copies run on two copy streams overlapped with compute (next step's inputs into a "
-            "second device buffer; this step's result snapshotted on the device, then read back)")
+            "second device buffer; this step's result snapshotted on the device into one of two buffers, then "
+            "read back)")
 
 
 # ------------------------------------------------------------------ GPU arm
