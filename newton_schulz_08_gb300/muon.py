@@ -220,6 +220,46 @@ def muon_step(params, grads, bufs, lr=0.02, momentum=0.95, nesterov=True, ns_ste
     return workspace
 
 
+class StepGraph:
+    """One muon_step recorded in a CUDA graph for fixed tensors, scalars and
+    workspace; replay() runs the step's launches (momentum pass, normalise,
+    the Newton-Schulz launches) with one host call.  The recording itself
+    runs nothing: params and bufs are first changed by the first replay.
+    The graph holds the tensors' addresses, so they must stay alive and in
+    place; a change of lr, momentum or ns_steps needs a new StepGraph.
+    Kernel-event recording (muon_set_debug "record_kernel_events") must be
+    off while recording."""
+
+    def __init__(self, params, grads, bufs, lr=0.02, momentum=0.95, nesterov=True, ns_steps=5, workspace=None):
+        self.tensors = (list(params), list(grads), list(bufs))
+        arr, n = _descs(*self.tensors)
+        if n == 0:
+            raise ValueError("StepGraph needs at least one matrix")
+        dev = _device_of(self.tensors[0] + self.tensors[1] + self.tensors[2]
+                         + ([workspace] if workspace is not None else []), "StepGraph")
+        with torch.cuda.device(dev):
+            if workspace is None:
+                workspace = new_workspace(lib().muon_workspace_size(arr, n), dev)
+            self.workspace = workspace
+            self.stream = torch.cuda.Stream(dev)
+            self.graph = torch.cuda.CUDAGraph()
+            self.stream.wait_stream(torch.cuda.current_stream(dev))
+            # relaxed: the first call of a bank also sets kernel attributes and
+            # queries occupancy, which are not stream work
+            with torch.cuda.graph(self.graph, stream=self.stream, capture_error_mode="relaxed"):
+                muon_step(params, grads, bufs, lr=lr, momentum=momentum, nesterov=nesterov, ns_steps=ns_steps,
+                          workspace=workspace, stream=self.stream)
+
+    def replay(self):
+        """Runs the recorded step (on the graph's stream, ordered after the
+        current stream's work so far; the current stream waits for it)."""
+        cur = torch.cuda.current_stream(self.stream.device)
+        self.stream.wait_stream(cur)
+        with torch.cuda.stream(self.stream):
+            self.graph.replay()
+        cur.wait_stream(self.stream)
+
+
 def ns5_workspace_size(batch, rows, cols):
     return lib().ns5_workspace_size(int(batch), int(rows), int(cols))
 

@@ -386,6 +386,31 @@ def test_last_update_of_a_bank_beyond_the_streamed_maps():
     assert bad == 0, bad
 
 
+def test_step_graph_replay_equals_eager():
+    """A step recorded in a CUDA graph changes nothing while it is recorded,
+    and two replays give the parameters and buffers of two eager steps bit
+    for bit (wide, tall and square matrices)."""
+    shapes = [(256, 256), (300, 100), (128, 512), (768, 3072)]
+    dev = torch.device("cuda")
+    P0 = [torch.from_numpy(inputs.param(s, 600 + i)).to(dev) for i, s in enumerate(shapes)]
+    B0 = [torch.from_numpy(inputs.buffer(s, 600 + i)).to(dev) for i, s in enumerate(shapes)]
+    G = [torch.from_numpy(inputs.grad(s, 600 + i)).to(dev).to(torch.bfloat16) for i, s in enumerate(shapes)]
+    Pg, Bg = [p.clone() for p in P0], [b.clone() for b in B0]
+    Pe, Be = [p.clone() for p in P0], [b.clone() for b in B0]
+    sg = muon.StepGraph(Pg, G, Bg, lr=0.02, momentum=0.95, nesterov=True, ns_steps=5)
+    torch.cuda.synchronize()
+    assert all(torch.equal(a, b) for a, b in zip(Pg, P0)) and all(torch.equal(a, b) for a, b in zip(Bg, B0))
+    ws = None
+    for _ in range(2):
+        sg.replay()
+        ws = muon.muon_step(Pe, G, Be, lr=0.02, momentum=0.95, nesterov=True, ns_steps=5, workspace=ws)
+    torch.cuda.synchronize()
+    check_status(sg.workspace)
+    check_status(ws)
+    for a, b in zip(Pg + Bg, Pe + Be):
+        assert torch.equal(a, b)
+
+
 def test_zero_lr_and_zero_momentum():
     """lr = 0 leaves the parameters bit for bit; momentum 0 makes the buffer
     the gradient (fp32 value of the bf16 gradient)."""
