@@ -28,7 +28,7 @@ namespace muon {
 namespace {
 
 constexpr int kEwThreads = 256;
-constexpr int kNormBatch = 4;  // normalise: 8-element vectors per thread in flight
+constexpr int kNormBatch = 8;  // normalise: 8-element vectors per thread in flight (four blocks per SM)
 constexpr int kCastBatch = 8;  // cast-only momentum pass: 8-element vectors per thread in flight
 constexpr int kMomBatch = 2;
 // Tall momentum pass: the 64 x 64 fp32 shared tile has rows of 66 floats and
@@ -432,7 +432,7 @@ __global__ void __launch_bounds__(kEwThreads, 4) momentum_cast_kernel(const __gr
   if (threadIdx.x == 0) P.partials[M.part_off + b] = s;
 }
 
-__global__ void __launch_bounds__(kEwThreads, 5) normalise_kernel(const __grid_constant__ NormParams P) {
+__global__ void __launch_bounds__(kEwThreads, 4) normalise_kernel(const __grid_constant__ NormParams P) {
   ptx_grid_dep_wait();
   __shared__ float red[kEwThreads / 32];
   __shared__ float sh_d;
