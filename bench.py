@@ -702,7 +702,7 @@ def main():
 
     # ------------------------------------------------------------- e2e
     out_host = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in e2e_out]
-    e_steps = max(3, args.steps // 4)
+    e_steps = max(10, args.steps // 2)
     barrier()
     e2e_ms = e2e_pipelined(stream, device, e_steps, e2e_in, e2e_host, e2e_step, e2e_out, out_host)
     barrier()
@@ -844,7 +844,7 @@ def run_sharded(args, rank, world, device):
     # parameters out, every step (serialised with the step)
     g_host = [f.cpu().pin_memory() for f in bank.grad_flat]
     p_host = [torch.empty(f.shape, dtype=f.dtype).pin_memory() for f in bank.param_flat]
-    e_steps = max(3, args.steps // 4)
+    e_steps = max(10, args.steps // 2)
     barrier()
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record(stream)
@@ -948,7 +948,7 @@ def run_adam(args, rank, world, device):
     p_host = [torch.empty(p.shape, dtype=p.dtype).pin_memory() for p in P]
     G2 = [torch.empty_like(g) for g in G]
     Gsets = [G, G2]
-    e_steps = max(3, args.steps // 4)
+    e_steps = max(10, args.steps // 2)
     k0 = args.warmup + args.steps
 
     def e2e_step(j):
