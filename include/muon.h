@@ -232,10 +232,19 @@ int muon_kernel_times(double* ms, int* launches, int n_kinds);
  * must start at zero); calls that may overlap on the GPU -- on different
  * streams or different host threads -- race on it and must be serialised by
  * the caller.  Allocates nothing: no cudaMalloc, cudaFree or allocating
- * library routine.  muon_device_status() is not available for these calls
- * (the status word is inside the private array). */
+ * library routine.  The device status word lives inside the private array:
+ * read it with ns5_noalloc_status, not muon_device_status. */
 muon_status_t ns5_noalloc(const void* G, int g_dtype, void* O, int batch, int64_t rows,
                           int64_t cols, int ns_steps, void* stream);
+
+/* Device status of the last ns5_noalloc call on the current device, as
+ * muon_device_status reports a workspace's: synchronises `stream` (the
+ * stream of that call), then returns MUON_OK, MUON_WARN_NONFINITE (a matrix
+ * had a non-finite norm) or MUON_ERR_DEVICE_TIMEOUT (a bounded wait
+ * expired, O is not valid).  MUON_ERR_UNSUPPORTED_DEVICE or MUON_ERR_CUDA
+ * when the array cannot be found.  Allocates nothing (the word is copied
+ * into a host variable). */
+muon_status_t ns5_noalloc_status(void* stream);
 
 /* One tensor of an Adam step: caller-owned DEVICE memory, contiguous. */
 typedef struct adam_tensor_desc {

@@ -74,3 +74,13 @@ extern "C" muon_status_t ns5_noalloc(const void* G, int g_dtype, void* O, int ba
   if (s != MUON_OK) return s;
   return ns5(G, g_dtype, O, batch, rows, cols, ns_steps, ws, kScratchBytes, stream);
 }
+
+// The status word of the last ns5_noalloc call on the current device: the
+// first word of the scratch array, read the way muon_device_status reads a
+// workspace's (a copy into a host variable, then the stream is waited for).
+extern "C" muon_status_t ns5_noalloc_status(void* stream) {
+  void* ws = nullptr;
+  const muon_status_t s = scratch_address(&ws);
+  if (s != MUON_OK) return s;
+  return muon_device_status(ws, stream);
+}

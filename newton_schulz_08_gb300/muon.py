@@ -34,7 +34,7 @@ MUON_F32 = 1
 #: every symbol include/muon.h declares
 EXPORTS = ["muon_workspace_size", "muon_step", "ns5_workspace_size", "ns5", "ns5_bank",
            "ns5_bank_workspace_size", "muon_device_status", "muon_status_str",
-           "ns5_workspace_layout", "muon_set_debug", "muon_kernel_times", "ns5_noalloc",
+           "ns5_workspace_layout", "muon_set_debug", "muon_kernel_times", "ns5_noalloc", "ns5_noalloc_status",
            "muon_partition", "adam_step", "fp8_mm", "muon_plan_cache_clear",
            "fp8_mm_backward", "fp8_mm_backward_workspace_size", "muon_debug_check_failures"]
 
@@ -115,6 +115,8 @@ def load(path):
     L.muon_kernel_times.restype = c_int
     L.ns5_noalloc.argtypes = [c_vp, c_int, c_vp, c_int, c_i64, c_i64, c_int, c_vp]
     L.ns5_noalloc.restype = c_int
+    L.ns5_noalloc_status.argtypes = [c_vp]
+    L.ns5_noalloc_status.restype = c_int
     L.muon_partition.argtypes = [P(c_i64), P(c_i64), c_int, c_int, P(c_int)]
     L.muon_partition.restype = c_int
     L.adam_step.argtypes = [P(adam_tensor_desc), c_int, c_f, c_f, c_f, c_f, c_f, c_int, c_int, c_vp]
@@ -376,6 +378,14 @@ def ns5_noalloc(G, ns_steps=5, out=None, stream=None):
                                _stream(stream))
     _check(st, "ns5_noalloc")
     return out[0] if squeeze else out
+
+
+def ns5_noalloc_status(stream=None, device=None):
+    """Device status of the last ns5_noalloc call on `device` (default: the
+    current one), read after synchronising `stream`: MUON_OK,
+    MUON_WARN_NONFINITE or MUON_ERR_DEVICE_TIMEOUT (see include/muon.h)."""
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        return lib().ns5_noalloc_status(_stream(stream))
 
 
 def partition(shapes, world):

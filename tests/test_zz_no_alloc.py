@@ -73,3 +73,33 @@ def test_noalloc_calls_allocate_no_device_memory():
     torch.cuda.synchronize()
     assert torch.cuda.memory_allocated() == held
     assert torch.cuda.mem_get_info()[0] == free
+
+
+@pytest.mark.gpu
+def test_noalloc_status_reports_ok_nonfinite_and_timeout():
+    """ns5_noalloc_status reads the status word inside the static array: OK
+    after a finite call, the non-finite warning after a NaN input, the
+    timeout after a call whose MMA warp issues nothing (bounded waits, ~10 ms),
+    and OK again after a finite call."""
+    rng = np.random.default_rng(11)
+    G = torch.from_numpy(rng.standard_normal((1, 256, 512)).astype(np.float32)).cuda()
+    out = torch.empty(G.shape, dtype=torch.bfloat16, device="cuda")
+    assert call_noalloc(G, out) == muon.MUON_OK
+    assert muon.ns5_noalloc_status() == muon.MUON_OK
+    Gn = G.clone()
+    Gn[0, 3, 5] = float("nan")
+    assert call_noalloc(Gn, out) == muon.MUON_OK
+    assert muon.ns5_noalloc_status() == muon.MUON_WARN_NONFINITE
+    muon.muon_set_debug("inject_stall", 1)
+    muon.muon_set_debug("wait_budget_cycles", 20_000_000)
+    try:
+        st = call_noalloc(G, out, ns_steps=1)
+        status = muon.ns5_noalloc_status()
+    finally:
+        muon.muon_set_debug("inject_stall", 0)
+        muon.muon_set_debug("wait_budget_cycles", 4_000_000_000)
+    assert st == muon.MUON_OK
+    assert status == muon.MUON_ERR_DEVICE_TIMEOUT
+    assert call_noalloc(G, out) == muon.MUON_OK
+    assert muon.ns5_noalloc_status() == muon.MUON_OK
+    assert torch.equal(out, muon.ns5(G, 5))
