@@ -30,14 +30,14 @@ namespace {
 constexpr int kEwThreads = 256;
 constexpr int kNormBatch = 8;  // normalise: 8-element vectors per thread in flight (four blocks per SM)
 constexpr int kCastBatch = 8;  // cast-only momentum pass: 8-element vectors per thread in flight
-constexpr int kMomBatch = 2;
+constexpr int kMomBatch = 2;   // momentum pass with bf16 G: 8-element vectors per thread in flight
 // Tall momentum pass: the 64 x 64 fp32 shared tile has rows of 66 floats and
 // column c of row r stored at c ^ (8 * ((r / 16) % 4)).  A warp's writes (two
 // rows, four consecutive columns per lane, the upper half-warp's in rotated
 // order) and its reads (column cc of rows rb + 2j, rb a multiple of 16) then
 // fall in 32 different banks.
 constexpr int kTallPitch = 66;
-__device__ __forceinline__ int tall_col(int r, int c) { return c ^ (((r >> 4) & 3) << 3); }   // momentum pass with bf16 G: 8-element vectors per thread in flight
+__device__ __forceinline__ int tall_col(int r, int c) { return c ^ (((r >> 4) & 3) << 3); }
 
 // Programmatic dependent launch: wait for the previous grid's results, then
 // let the next grid be scheduled.
