@@ -437,9 +437,13 @@ __global__ void __launch_bounds__(kEwThreads, 4) normalise_kernel(const __grid_c
   __shared__ float red[kEwThreads / 32];
   __shared__ float sh_d;
   int c = 0;
-  while (c + 1 < P.n_classes && (int)blockIdx.x >= P.cls[c + 1].block_begin) ++c;
+  // blocks run in reverse order of the momentum pass's: the rows that pass
+  // wrote last are read first, while they are still in L2 (56.0 -> 52.0 us on
+  // the GPT-2 bank)
+  const int bid = static_cast<int>(gridDim.x - 1 - blockIdx.x);
+  while (c + 1 < P.n_classes && bid >= P.cls[c + 1].block_begin) ++c;
   const NormClass& K = P.cls[c];
-  const int local = blockIdx.x - K.block_begin;
+  const int local = bid - K.block_begin;
   const int idx = local / K.blocks_per_mat;
   const int b = local - idx * K.blocks_per_mat;
   // debug build: the block's rows lie inside its class and matrix
