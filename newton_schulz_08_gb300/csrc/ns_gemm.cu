@@ -74,11 +74,10 @@ struct Tile {
 
 template <int MODE>
 __device__ __forceinline__ Tile decode_tile(const GemmParams& P, int t) {
-  // The Gram and update launches walk their tile lists from the end: more of
-  // the data the previous launch wrote last is still in L2 when it is read
-  // (GPT-2 bank: step 1.300 -> 1.291 ms).  Every role of a CTA decodes the
-  // same sequence, so the order is all that changes.
-  if (MODE == kGram || MODE == kUpdate) t = P.total_tiles - 1 - t;
+  // A launch may walk its tile list from the end (the planner's choice, for
+  // L2 reuse of what the previous launch wrote last).  Every role of a CTA
+  // decodes the same sequence, so the order is all that changes.
+  if (P.reverse) t = P.total_tiles - 1 - t;
   int c = 0;
 #pragma unroll 1
   while (c + 1 < P.n_classes && t >= P.cls[c + 1].tile_begin) ++c;

@@ -165,6 +165,7 @@ struct GemmParams {
   float lr;                     //   the matrices' parameters and the rate
   int apply;                    // 1: the epilogue applies p <- p - lr X' (fp32,
                                 //   in p's own layout) instead of storing X'
+  int reverse;                  // 1: the tile list is walked from its end
 };
 
 // The Muon step's last update with the parameters streamed through shared
