@@ -1122,7 +1122,7 @@ def run_fp8(args, rank, world, device):
     bufs = [[X, W], [torch.empty_like(X), torch.empty_like(W)]]
     o_host = [torch.empty(O.shape, dtype=O.dtype).pin_memory()]
     barrier()
-    e2e_ms = e2e_pipelined(stream, device, max(3, args.steps // 4), bufs, in_host,
+    e2e_ms = e2e_pipelined(stream, device, max(10, args.steps // 2), bufs, in_host,
                            lambda j: step(bufs[j][0], bufs[j][1]), [O], o_host)
     barrier()
     clk = clocks.stop()
